@@ -1,0 +1,491 @@
+#!/usr/bin/env python
+"""Benchmark of the paged KV-cache transfer on GB300.
+
+One step = the whole hot path over one batch: the all-layer D2H backup of the
+workload's pages, then the per-layer H2D load-back burst of those pages into
+fresh device pages with one layer-done event per layer.  The headline metric
+is KV transfer GB/s (payload bytes of both operations / device time) and its
+fraction of the host-link peak measured in the same run with pinned
+cudaMemcpyAsync copies (D2H and H2D, 1 GiB, best of 5).
+
+Default workload: the Llama-3-8B-shaped MHA pool (32 layers, 8x128 bf16 K/V,
+page_size 64; backup of 256 pages = 2 GiB, then load-back of 256 pages =
+64 MiB per layer).  Pools are 8 GiB on each side, larger than L2, so no flush
+is needed between steps.
+
+Multi-GPU: every pair is independent and each GPU holds its own pool replica,
+so N ranks run N independent replicas (weak scaling, no collective on the data
+path); rank 0 prints the aggregate.
+
+``--impl reference`` times the CPU oracle (plain C loops) on a bounded sample
+of the same workload, the only baseline that exists for this path.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+import numpy as np
+
+REPO = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, REPO)
+
+METRIC = "KV transfer GB/s (D2H backup, H2D per-layer load) & % of measured host-link peak"
+UNIT = "GB/s"
+GB = 1e9
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama3_8b_mha")
+    ap.add_argument("--path", choices=["auto", "zero_copy", "staged"], default="auto")
+    ap.add_argument("--staging-mib", type=int, default=256)
+    ap.add_argument("--max-ctas", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--out", default=None, help="also append the JSON line to this file")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- distributed
+
+def dist_setup(n_gpus):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return rank, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for ln in open(self.path):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- host link peak
+
+def measure_link_peak(nbytes=1 << 30, reps=5):
+    import torch
+    h = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    d = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    h.fill_(1)
+    d.fill_(2)
+    s = torch.cuda.Stream()
+    out = {}
+    for name, dst, src in (("d2h", h, d), ("h2d", d, h)):
+        best = 0.0
+        with torch.cuda.stream(s):
+            for r in range(reps + 1):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(s)
+                dst.copy_(src, non_blocking=True)
+                e1.record(s)
+                e1.synchronize()
+                if r:
+                    best = max(best, nbytes / (e0.elapsed_time(e1) * 1e-3) / GB)
+        out[name] = best
+    del h, d
+    torch.cuda.synchronize()
+    return out
+
+
+# ---------------------------------------------------------------- workload
+
+def build_workload(name, seed_offset=0):
+    from hierarchical_kv_cache_gb300 import workloads as W
+    wl = W.WORKLOADS[name]()
+    s0 = wl.pools[0]
+    P = s0.page_size
+    dev_pages = min(s.device_slots for s in wl.pools) // P
+    host_pages = min(s.host_pages for s in wl.pools)
+    d, h, dp, _ = W.page_pairs(wl.seed + seed_offset, wl.move_pages, dev_pages, host_pages, P)
+    d2, _, _, _ = W.page_pairs(wl.seed + seed_offset + 1, wl.move_pages, dev_pages, host_pages, P,
+                               exclude_device_pages=dp)
+    return wl, d, h, d2
+
+
+def payload_bytes(wl, n):
+    backup = sum(n * s.num_layers * s.num_tensors * s.row_bytes for s in wl.pools)
+    per_layer = sum(n * s.num_tensors * s.row_bytes for s in wl.pools)
+    return backup, per_layer
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world):
+    import torch
+    import hierarchical_kv_cache_gb300 as hk
+    from hierarchical_kv_cache_gb300 import pools as hpools
+    from hierarchical_kv_cache_gb300.build import build
+
+    build()
+    wl, d, h, d2 = build_workload(args.workload)
+    L = wl.pools[0].num_layers
+    n = d.size
+    t_alloc = time.time()
+    pools = []
+    for i, s in enumerate(wl.pools):
+        p = hpools.allocate_pool(s)
+        hpools.fill_device_random_(p, wl.seed + i, s.value_kind)
+        for ht in p.host_tensors:
+            ht.zero_()
+        pools.append(p)
+    torch.cuda.synchronize()
+    t_alloc = time.time() - t_alloc
+
+    path = {"auto": hk.HICACHE_PATH_AUTO, "zero_copy": hk.HICACHE_PATH_ZERO_COPY,
+            "staged": hk.HICACHE_PATH_STAGED}[args.path]
+    staging = None
+    if args.path != "zero_copy":
+        staging = [torch.empty(args.staging_mib << 20, dtype=torch.uint8, device="cuda")
+                   for _ in range(2)]
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.Stream()
+
+    # device-resident indices for the device-timed value
+    dt = torch.as_tensor(d).cuda()
+    ht_dev = torch.as_tensor(h).cuda()
+    d2t = torch.as_tensor(d2).cuda()
+    # pinned host indices for the end-to-end leg and the staged path
+    dt_h = torch.as_tensor(d).pin_memory()
+    ht_h = torch.as_tensor(h).pin_memory()
+    d2t_h = torch.as_tensor(d2).pin_memory()
+    if args.path == "staged":
+        idx_b, idx_l = (dt_h, ht_h), (ht_h, d2t_h)
+        opts = hk.Opts(path=path, index_location=hk.HICACHE_INDEX_HOST, staging=staging,
+                       max_ctas=args.max_ctas, device_error=err)
+    else:
+        idx_b, idx_l = (dt, ht_dev), (ht_dev, d2t)
+        opts = hk.Opts(path=path, index_location=hk.HICACHE_INDEX_DEVICE, staging=staging,
+                       max_ctas=args.max_ctas, device_error=err)
+
+    link = measure_link_peak()
+    bytes_backup, bytes_layer = payload_bytes(wl, n)
+    bytes_load = bytes_layer * L
+    step_bytes = bytes_backup + bytes_load
+
+    def step(layer_events, enqueue_times=None):
+        hk.hicache_backup_all_layers(pools, idx_b[0], idx_b[1], opts=opts, stream=stream)
+        t0 = time.perf_counter()
+        hk.hicache_load_burst(pools, 0, L, idx_l[0], idx_l[1], opts=opts, stream=stream,
+                              layer_done=layer_events)
+        if enqueue_times is not None:
+            enqueue_times.append(time.perf_counter() - t0)
+
+    # warm-up
+    warm_events = [torch.cuda.Event(enable_timing=True) for _ in range(L)]
+    for _ in range(args.warmup):
+        step(warm_events)
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_m = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_layers = [[torch.cuda.Event(enable_timing=True) for _ in range(L)] for _ in range(K)]
+    enq = []
+    launches0 = hk.kernel_launches()
+    clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    barrier(world)
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    wall0 = time.perf_counter()
+    for k in range(K):
+        ev_s[k].record(stream)
+        hk.hicache_backup_all_layers(pools, idx_b[0], idx_b[1], opts=opts, stream=stream)
+        ev_m[k].record(stream)
+        t0 = time.perf_counter()
+        hk.hicache_load_burst(pools, 0, L, idx_l[0], idx_l[1], opts=opts, stream=stream,
+                              layer_done=ev_layers[k])
+        enq.append(time.perf_counter() - t0)
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop() if clocks else None
+    launches = hk.kernel_launches() - launches0
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error word {int(err.item())}")
+
+    total_ms = ev_s[0].elapsed_time(ev_layers[-1][-1])
+    t_backup = [ev_s[k].elapsed_time(ev_m[k]) for k in range(K)]
+    t_load = [ev_m[k].elapsed_time(ev_layers[k][-1]) for k in range(K)]
+    t_first = [ev_m[k].elapsed_time(ev_layers[k][0]) for k in range(K)]
+    per_layer = [ev_layers[k][l - 1].elapsed_time(ev_layers[k][l]) for k in range(K)
+                 for l in range(1, L)]
+    total_ms = max_over_ranks(total_ms, world)
+    value = world * K * step_bytes / (total_ms * 1e-3) / GB
+
+    mb, ml = statistics.mean(t_backup), statistics.mean(t_load)
+    backup_gbs = bytes_backup / (mb * 1e-3) / GB
+    load_gbs = bytes_load / (ml * 1e-3) / GB
+    layer_gbs = bytes_layer / (statistics.median(per_layer) * 1e-3) / GB if per_layer else None
+    first_us = statistics.mean(t_first) * 1e3
+    bound_us = ml * 1e3 / L + 20.0
+    # time-weighted link peak of the step's mix of directions
+    peak_mix = step_bytes / (bytes_backup / link["d2h"] + bytes_load / link["h2d"])
+    achieved = step_bytes / ((mb + ml) * 1e-3) / GB
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(hk, pools, wl, dt_h, ht_h, d2t_h, L, staging, path, args, step_bytes, n)
+
+    res = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / K, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u8 (opaque bf16 KV bytes)",
+        "data": "synthetic (seeded bf16 ~N(0,1) pools, seeded random page lists)",
+        "config": {
+            "workload": wl.name, "description": wl.description,
+            "pages_per_op": wl.move_pages, "tokens_per_op": int(n), "layers": L,
+            "step": "all-layer D2H backup + H2D per-layer load-back burst with layer events",
+            "step_payload_bytes": int(step_bytes), "path": args.path,
+            "index_location": "device (HBM)" if args.path != "staged" else "host (pinned)",
+            "l2": "inputs larger than L2 (8 GiB pools each side), no flush",
+            "parallelism": f"replicas x{world}",
+            "host_alloc_s": round(t_alloc, 1),
+        },
+        "ops": {
+            "backup_d2h_gbs": round(backup_gbs, 2),
+            "backup_frac_of_link_d2h": round(backup_gbs / link["d2h"], 4),
+            "backup_ms": round(mb, 4),
+            "load_h2d_gbs": round(load_gbs, 2),
+            "load_frac_of_link_h2d": round(load_gbs / link["h2d"], 4),
+            "load_burst_ms": round(ml, 4),
+            "load_per_layer_median_gbs": round(layer_gbs, 2) if layer_gbs else None,
+            "first_layer_event_us": round(first_us, 1),
+            "first_event_bound_us": round(bound_us, 1),
+            "first_event_within_bound": first_us <= bound_us,
+            "enqueue_us_per_layer": round(statistics.median(enq) * 1e6 / L, 2),
+            "link_peak_gbs": {k: round(v, 2) for k, v in link.items()},
+        },
+        "roofline": {
+            "bound": "host_link", "achieved": round(achieved, 2), "peak": round(peak_mix, 2),
+            "unit": "GB/s", "frac": round(achieved / peak_mix, 4), "traffic": None,
+            "kernel": "row_copy_kernel (all launches of one step)",
+            "peak_source": "pinned cudaMemcpyAsync D2H/H2D measured in this run, weighted by "
+                           "the step's bytes per direction",
+        },
+        "gpu_launches": int(launches),
+        "clocks": clk,
+        "e2e": e2e,
+        "wall_s_timed": round(wall, 3),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(wl, d, h, d2, args.cpu_seconds)
+    return res
+
+
+def run_e2e(hk, pools, wl, dt_h, ht_h, d2t_h, L, staging, path, args, step_bytes, n):
+    """Public-API step with pinned host indices (host validation included) and a D2H status read."""
+    import torch
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    err_h = torch.zeros(1, dtype=torch.int32).pin_memory()
+    opts = hk.Opts(path=path, index_location=hk.HICACHE_INDEX_HOST, staging=staging,
+                   max_ctas=args.max_ctas, device_error=err)
+    events = [torch.cuda.Event() for _ in range(L)]
+    stream = torch.cuda.Stream()
+
+    def one():
+        hk.hicache_backup_all_layers(pools, dt_h, ht_h, opts=opts, stream=stream)
+        hk.hicache_load_burst(pools, 0, L, ht_h, d2t_h, opts=opts, stream=stream,
+                              layer_done=events)
+        with torch.cuda.stream(stream):
+            err_h.copy_(err, non_blocking=True)
+        stream.synchronize()
+        if int(err_h.item()) != 0:
+            raise RuntimeError("device error in e2e step")
+
+    for _ in range(2):
+        one()
+    K = max(3, args.steps // 2)
+    t0 = time.perf_counter()
+    for _ in range(K):
+        one()
+    dt = (time.perf_counter() - t0) / K
+    idx_bytes = 3 * n * 8
+    bytes_backup, bytes_layer = payload_bytes(wl, n)
+    return {"value": round(step_bytes / dt / GB, 2), "unit": UNIT,
+            "h2d_bytes_per_step": int(bytes_layer * L + idx_bytes),
+            "d2h_bytes_per_step": int(bytes_backup + 4),
+            "note": "host wall clock per step; pinned host indices validated on the CPU each "
+                    "call; payload crosses the host link by definition of the op"}
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def oracle_step_sample(wl, d, h, d2, pages, dev_imgs, host_imgs):
+    """One oracle pass over the first `pages` pages of the step: backup then load burst."""
+    import oracle
+    P = wl.pools[0].page_size
+    m = pages * P
+    nbytes = 0
+    for s, dimg, himg in zip(wl.pools, dev_imgs, host_imgs):
+        for t in range(s.num_tensors):
+            oracle.backup_all_layers(dimg[t], himg[t], d[:m], h[:m], page_size=P,
+                                     row_bytes=s.row_bytes)
+            oracle.load_burst(dimg[t], himg[t], 0, s.num_layers, h[:m], d2[:m], page_size=P,
+                              row_bytes=s.row_bytes)
+            nbytes += 2 * m * s.num_layers * s.row_bytes
+    return nbytes
+
+
+def oracle_images(wl):
+    dev, host = [], []
+    for s in wl.pools:
+        dev.append([[np.empty(s.device_slots * s.row_bytes, dtype=np.uint8)
+                     for _ in range(s.num_layers)] for _ in range(s.num_tensors)])
+        host.append([np.empty(s.host_pages * s.num_layers * s.page_size * s.row_bytes,
+                              dtype=np.uint8) for _ in range(s.num_tensors)])
+    return dev, host
+
+
+def cpu_baseline(wl, d, h, d2, seconds):
+    dev_imgs, host_imgs = oracle_images(wl)
+    pages = max(1, min(wl.move_pages, 32))
+    oracle_step_sample(wl, d, h, d2, pages, dev_imgs, host_imgs)  # touch the pages once
+    total, t0 = 0, time.perf_counter()
+    reps = 0
+    while time.perf_counter() - t0 < seconds:
+        total += oracle_step_sample(wl, d, h, d2, pages, dev_imgs, host_imgs)
+        reps += 1
+    dt = time.perf_counter() - t0
+    return {"value": round(total / dt / GB, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{pages} of {wl.move_pages} pages per pass (backup + load of all layers), "
+                      f"{reps} passes, {dt:.1f} s, plain C memcpy loops on one host core"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    wl, d, h, d2 = build_workload(args.workload)
+    dev_imgs, host_imgs = oracle_images(wl)
+    pages = max(1, min(wl.move_pages, 16))
+    for _ in range(args.warmup):
+        oracle_step_sample(wl, d, h, d2, pages, dev_imgs, host_imgs)
+    total, t0 = 0, time.perf_counter()
+    for _ in range(args.steps):
+        total += oracle_step_sample(wl, d, h, d2, pages, dev_imgs, host_imgs)
+    dt = time.perf_counter() - t0
+    v = round(total / dt / GB, 3)
+    return {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+        "data": "synthetic", "config": {"workload": wl.name, "path": "cpu oracle"},
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{pages} of {wl.move_pages} pages per step, all layers, "
+                                   "backup + load"},
+        "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        res = run_reference(args, rank, world)
+    else:
+        rank, world = dist_setup(args.gpus)
+        res = run_ours(args, rank, world)
+    if res is not None and rank == 0:
+        line = json.dumps(res)
+        print(line, flush=True)
+        if args.out:
+            with open(args.out, "a") as f:
+                f.write(line + "\n")
+    if args.impl != "reference" and world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,287 @@
+"""Thin ctypes binding of ``libhicache_gb300.so`` (include/hicache.h).
+
+Argument marshalling only: every byte is moved by the library's CUDA kernels or
+its copy-engine DMA.  Torch supplies device memory, pinned host memory,
+streams and events.  The functions keep the C names and raise ``HiCacheError``
+for a non-OK status.  If the library has not been built, every call raises
+``RuntimeError``; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass, field
+from typing import Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libhicache_gb300.so")
+
+HICACHE_OK, HICACHE_EINVAL, HICACHE_ERANGE, HICACHE_EDUP, HICACHE_EALIGN, HICACHE_ECUDA, \
+    HICACHE_ENOSTAGE = range(7)
+STATUS_NAMES = {0: "HICACHE_OK", 1: "HICACHE_EINVAL", 2: "HICACHE_ERANGE", 3: "HICACHE_EDUP",
+                4: "HICACHE_EALIGN", 5: "HICACHE_ECUDA", 6: "HICACHE_ENOSTAGE"}
+HICACHE_PATH_AUTO, HICACHE_PATH_ZERO_COPY, HICACHE_PATH_STAGED = 0, 1, 2
+HICACHE_INDEX_HOST, HICACHE_INDEX_DEVICE = 0, 1
+HICACHE_DEVERR_RANGE, HICACHE_DEVERR_PAGE_ALIGN = 1, 2
+
+
+class c_pool(ctypes.Structure):
+    _fields_ = [("num_layers", ctypes.c_int32), ("num_tensors", ctypes.c_int32),
+                ("head_num", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("dtype_size", ctypes.c_int32), ("page_size", ctypes.c_int32),
+                ("page_granular", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("device_slots", ctypes.c_int64), ("host_pages", ctypes.c_int64),
+                ("device_layers", ctypes.POINTER(ctypes.c_void_p)),
+                ("host_tensors", ctypes.POINTER(ctypes.c_void_p))]
+
+
+class c_opts(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int32), ("index_location", ctypes.c_int32),
+                ("max_ctas", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("staging", ctypes.c_void_p * 2), ("staging_bytes", ctypes.c_size_t),
+                ("copy_stream", ctypes.c_void_p), ("device_error", ctypes.c_void_p)]
+
+
+class c_run(ctypes.Structure):
+    _fields_ = [("d0", ctypes.c_int64), ("h0", ctypes.c_int64), ("len", ctypes.c_int64)]
+
+
+_lib = None
+
+
+def lib():
+    """The loaded C library; raises if it was not built (no fallback exists)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "hierarchical_kv_cache_gb300.build.build() (nvcc, sm_103a)")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+        P = ctypes.POINTER(c_pool)
+        O = ctypes.POINTER(c_opts)
+        L.hicache_backup_all_layers.argtypes = [P, i32, vp, vp, i32, i64, O, vp]
+        L.hicache_load_layer.argtypes = [P, i32, i32, vp, vp, i32, i64, O, vp, vp]
+        L.hicache_load_burst.argtypes = [P, i32, i32, i32, vp, vp, i32, i64, O, vp,
+                                         ctypes.POINTER(vp)]
+        L.hicache_plan_runs.argtypes = [vp, vp, i32, i64, i32, ctypes.POINTER(c_run), i64,
+                                        ctypes.POINTER(i64), ctypes.POINTER(i64)]
+        L.hicache_layer_checksum.argtypes = [P, i32, i32, vp, i32, i64, vp, vp]
+        for f in ("hicache_backup_all_layers", "hicache_load_layer", "hicache_load_burst",
+                  "hicache_plan_runs", "hicache_layer_checksum"):
+            getattr(L, f).restype = ctypes.c_int
+        L.hicache_last_error.restype = ctypes.c_char_p
+        L.hicache_last_error.argtypes = []
+        L.hicache_abi_version.restype = ctypes.c_int32
+        L.hicache_abi_version.argtypes = []
+        L.hicache_kernel_launches.restype = ctypes.c_int64
+        L.hicache_kernel_launches.argtypes = []
+        _lib = L
+    return _lib
+
+
+class HiCacheError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+        self.message = message
+
+
+def _check(status: int):
+    if status != HICACHE_OK:
+        raise HiCacheError(status, lib().hicache_last_error().decode(errors="replace"))
+
+
+@dataclass
+class Pool:
+    """One KV pool: device layer buffers [tensor][layer] and pinned host tensors [tensor].
+
+    Any tensor dtype works; the library sees bytes.  device_layers[t][l] must
+    hold device_slots * row_bytes bytes and host_tensors[t] host_pages *
+    num_layers * page_size * row_bytes bytes.
+    """
+
+    device_layers: Sequence[Sequence]
+    host_tensors: Sequence
+    num_layers: int
+    head_num: int
+    head_dim: int
+    dtype_size: int
+    page_size: int
+    device_slots: int
+    host_pages: int
+    page_granular: bool = False
+    _keep: list = field(default_factory=list, repr=False)
+
+    @property
+    def num_tensors(self) -> int:
+        return len(self.host_tensors)
+
+    @property
+    def row_bytes(self) -> int:
+        return self.head_num * self.head_dim * self.dtype_size
+
+    def to_c(self) -> c_pool:
+        T, L = self.num_tensors, self.num_layers
+        dev = (ctypes.c_void_p * (T * L))(*[self.device_layers[t][l].data_ptr()
+                                            for t in range(T) for l in range(L)])
+        host = (ctypes.c_void_p * T)(*[h.data_ptr() for h in self.host_tensors])
+        self._keep = [dev, host]
+        return c_pool(num_layers=L, num_tensors=T, head_num=self.head_num,
+                      head_dim=self.head_dim, dtype_size=self.dtype_size,
+                      page_size=self.page_size, page_granular=int(self.page_granular),
+                      reserved=0, device_slots=self.device_slots, host_pages=self.host_pages,
+                      device_layers=ctypes.cast(dev, ctypes.POINTER(ctypes.c_void_p)),
+                      host_tensors=ctypes.cast(host, ctypes.POINTER(ctypes.c_void_p)))
+
+
+@dataclass
+class Opts:
+    """Mirror of hicache_opts; index_location None = inferred from the index tensors."""
+
+    path: int = HICACHE_PATH_AUTO
+    index_location: Optional[int] = None
+    max_ctas: int = 0
+    staging: Optional[Sequence] = None  # two device tensors
+    copy_stream: Optional[object] = None  # torch.cuda.Stream
+    device_error: Optional[object] = None  # int32/uint32 tensor of one element
+
+
+def _pools_arg(pools):
+    if not isinstance(pools, (list, tuple)):
+        pools = [pools]
+    arr = (c_pool * len(pools))(*[p.to_c() for p in pools])
+    return arr, len(pools), pools
+
+
+def _index_bits(t) -> int:
+    import torch
+    if t.dtype == torch.int32:
+        return 32
+    if t.dtype == torch.int64:
+        return 64
+    raise TypeError(f"index tensors must be int32 or int64, got {t.dtype}")
+
+
+def _opts_arg(opts: Optional[Opts], a, b):
+    o = opts or Opts()
+    loc = o.index_location
+    if loc is None:
+        loc = HICACHE_INDEX_DEVICE if a.is_cuda else HICACHE_INDEX_HOST
+    c = c_opts(path=o.path, index_location=loc, max_ctas=o.max_ctas, reserved=0)
+    if o.staging is not None:
+        c.staging[0] = o.staging[0].data_ptr()
+        c.staging[1] = o.staging[1].data_ptr()
+        c.staging_bytes = min(o.staging[0].numel() * o.staging[0].element_size(),
+                              o.staging[1].numel() * o.staging[1].element_size())
+    if o.copy_stream is not None:
+        c.copy_stream = o.copy_stream.cuda_stream
+    if o.device_error is not None:
+        c.device_error = o.device_error.data_ptr()
+    return c
+
+
+def _stream_arg(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _event_handle(ev, stream_handle) -> int:
+    """Raw cudaEvent_t of a torch event, creating it on first use."""
+    if ev is None:
+        return 0
+    h = ev.cuda_event
+    if h == 0:  # torch creates the CUDA event lazily, on its first record
+        ev.record()
+        h = ev.cuda_event
+    return h
+
+
+def _indices(a, b):
+    if a.numel() != b.numel():
+        raise ValueError("index tensors differ in length")
+    if a.device != b.device or a.dtype != b.dtype:
+        raise ValueError("index tensors must share device and dtype")
+    if not (a.is_contiguous() and b.is_contiguous()):
+        raise ValueError("index tensors must be contiguous")
+    return _index_bits(a), a.numel()
+
+
+def hicache_backup_all_layers(pools, device_indices, host_indices, *, opts: Optional[Opts] = None,
+                              stream=None) -> None:
+    """All-layer D2H backup of pairs device_indices[i] -> host_indices[i] (see hicache.h)."""
+    arr, npools, _ = _pools_arg(pools)
+    bits, n = _indices(device_indices, host_indices)
+    o = _opts_arg(opts, device_indices, host_indices)
+    _check(lib().hicache_backup_all_layers(arr, npools, device_indices.data_ptr(),
+                                           host_indices.data_ptr(), bits, n, ctypes.byref(o),
+                                           _stream_arg(stream)))
+
+
+def hicache_load_layer(pools, layer: int, host_indices, device_indices, *,
+                       opts: Optional[Opts] = None, stream=None, layer_done=None) -> None:
+    """H2D load-back of one layer; records ``layer_done`` (a torch.cuda.Event) after it."""
+    arr, npools, _ = _pools_arg(pools)
+    bits, n = _indices(device_indices, host_indices)
+    o = _opts_arg(opts, device_indices, host_indices)
+    s = _stream_arg(stream)
+    _check(lib().hicache_load_layer(arr, npools, layer, host_indices.data_ptr(),
+                                    device_indices.data_ptr(), bits, n, ctypes.byref(o), s,
+                                    _event_handle(layer_done, s)))
+
+
+def hicache_load_burst(pools, layer_begin: int, layer_end: int, host_indices, device_indices, *,
+                       opts: Optional[Opts] = None, stream=None, layer_done=None) -> None:
+    """H2D load-back of layers [layer_begin, layer_end), one event per layer (list or None)."""
+    arr, npools, _ = _pools_arg(pools)
+    bits, n = _indices(device_indices, host_indices)
+    o = _opts_arg(opts, device_indices, host_indices)
+    s = _stream_arg(stream)
+    count = max(0, layer_end - layer_begin)
+    evs = None
+    if layer_done is not None:
+        if len(layer_done) != count:
+            raise ValueError("layer_done must hold one event per layer")
+        evs = (ctypes.c_void_p * max(1, count))(*[_event_handle(e, s) for e in layer_done])
+    _check(lib().hicache_load_burst(arr, npools, layer_begin, layer_end, host_indices.data_ptr(),
+                                    device_indices.data_ptr(), bits, n, ctypes.byref(o), s, evs))
+
+
+def hicache_plan_runs(device_indices, host_indices, page_size: int):
+    """Maximal runs (d0, h0, len) of host-memory index arrays and the whole-page run count."""
+    d = np.ascontiguousarray(device_indices)
+    h = np.ascontiguousarray(host_indices)
+    if d.dtype != h.dtype or d.dtype not in (np.int32, np.int64) or d.shape != h.shape:
+        raise TypeError("index arrays must be equal-length int32 or int64")
+    bits = 32 if d.dtype == np.int32 else 64
+    count = ctypes.c_int64(0)
+    full = ctypes.c_int64(0)
+    _check(lib().hicache_plan_runs(d.ctypes.data, h.ctypes.data, bits, d.size, page_size, None, 0,
+                                   ctypes.byref(count), None))
+    runs = (c_run * max(1, count.value))()
+    _check(lib().hicache_plan_runs(d.ctypes.data, h.ctypes.data, bits, d.size, page_size, runs,
+                                   count.value, ctypes.byref(count), ctypes.byref(full)))
+    out = np.array([(r.d0, r.h0, r.len) for r in runs[:count.value]], dtype=np.int64)
+    return out.reshape(-1, 3), full.value
+
+
+def hicache_layer_checksum(pool: Pool, tensor: int, layer: int, device_indices, out_sum, *,
+                           stream=None) -> None:
+    """Adds the 32-bit words of the indexed rows into ``out_sum`` (a zeroed int64 CUDA tensor)."""
+    arr, _, _ = _pools_arg(pool)
+    bits = _index_bits(device_indices)
+    _check(lib().hicache_layer_checksum(arr, tensor, layer, device_indices.data_ptr(), bits,
+                                        device_indices.numel(), out_sum.data_ptr(),
+                                        _stream_arg(stream)))
+
+
+def abi_version() -> int:
+    return lib().hicache_abi_version()
+
+
+def kernel_launches() -> int:
+    """Kernels the library has launched in this process."""
+    return lib().hicache_kernel_launches()

@@ -1,0 +1,264 @@
+// api.cu -- the extern "C" entry points declared in include/hicache.h.
+//
+// Each entry point validates everything on the host first (no copy is
+// enqueued for a rejected call), resolves the device-visible addresses of the
+// pinned host buffers, picks a path and enqueues the copies on the caller's
+// stream.  Load calls record their layer-done events on every return path, the
+// error convention of "[HiCache] Run the host->device load-back enqueue on a
+// loader thread" (Modifications: a failed load completes every layer event).
+#include <cuda_runtime.h>
+
+#include <string>
+#include <vector>
+
+#include "hicache_internal.h"
+#include "staged.h"
+
+namespace hk {
+const std::string& last_error();
+
+namespace {
+
+hicache_opts default_opts() {
+  hicache_opts o{};
+  o.path = HICACHE_PATH_AUTO;
+  o.index_location = HICACHE_INDEX_HOST;
+  return o;
+}
+
+hicache_status check_opts(const hicache_opts& o) {
+  if (o.path < HICACHE_PATH_AUTO || o.path > HICACHE_PATH_STAGED)
+    return fail(HICACHE_EINVAL, "opts.path is not a hicache_path");
+  if (o.index_location != HICACHE_INDEX_HOST && o.index_location != HICACHE_INDEX_DEVICE)
+    return fail(HICACHE_EINVAL, "opts.index_location is not a hicache_index_location");
+  if (o.max_ctas < 0) return fail(HICACHE_EINVAL, "opts.max_ctas is negative");
+  if (o.reserved != 0) return fail(HICACHE_EINVAL, "opts.reserved must be 0");
+  return HICACHE_OK;
+}
+
+hicache_status cuda_fail(cudaError_t e, const std::string& what) {
+  return fail(HICACHE_ECUDA, what + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")");
+}
+
+enum class Want { kHostPinned, kDevice, kAny };
+
+// Device-visible address of `ptr`, checking where it lives.
+hicache_status device_view(const void* ptr, Want want, const std::string& what, const void** out) {
+  cudaPointerAttributes a{};
+  const cudaError_t e = cudaPointerGetAttributes(&a, ptr);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return cuda_fail(e, "cudaPointerGetAttributes(" + what + ")");
+  }
+  const bool host = a.type == cudaMemoryTypeHost;
+  const bool dev = a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+  if (want == Want::kHostPinned && !host)
+    return fail(HICACHE_EINVAL, what + " must be pinned (page-locked) host memory");
+  if (want == Want::kDevice && !dev) return fail(HICACHE_EINVAL, what + " must be device memory");
+  if (!host && !dev)
+    return fail(HICACHE_EINVAL, what + " is not memory the GPU can address (pin it first)");
+  *out = (host && a.devicePointer) ? a.devicePointer : ptr;
+  return HICACHE_OK;
+}
+
+struct Prepared {
+  std::vector<PoolInfo> pools;
+  hicache_opts o{};
+  IndexSet idx;
+};
+
+// Checks arguments and indices; resolves device-visible addresses.
+// When check_layers is set, [layer_begin, layer_end) must lie inside the pools' layers.
+hicache_status prepare(const hicache_pool* pools, int32_t num_pools, const void* dev_idx,
+                       const void* host_idx, int32_t bits, int64_t n, const hicache_opts* opts,
+                       bool dest_is_device, bool check_layers, int32_t layer_begin,
+                       int32_t layer_end, Prepared* out) {
+  out->o = opts ? *opts : default_opts();
+  hicache_status st = check_pools(pools, num_pools, &out->pools);
+  if (st != HICACHE_OK) return st;
+  if (check_layers) {
+    if (layer_begin < 0 || layer_end > out->pools[0].L || layer_begin > layer_end)
+      return fail(HICACHE_EINVAL, "layer range [" + std::to_string(layer_begin) + ", " +
+                                      std::to_string(layer_end) + ") outside the pools' " +
+                                      std::to_string(out->pools[0].L) + " layers");
+  }
+  st = check_opts(out->o);
+  if (st != HICACHE_OK) return st;
+  st = check_index_args(dev_idx, host_idx, bits, n);
+  if (st != HICACHE_OK) return st;
+  out->idx.bits = bits;
+  out->idx.n = n;
+  if (out->o.index_location == HICACHE_INDEX_HOST) {
+    out->idx.dev_cpu = dev_idx;
+    out->idx.host_cpu = host_idx;
+    st = check_pairs_host(out->pools, dev_idx, host_idx, bits, n, dest_is_device);
+    if (st != HICACHE_OK) return st;
+  }
+  if (n == 0) return HICACHE_OK;
+  // Host pool tensors: pinned memory (or device memory) the kernels can address.
+  for (size_t p = 0; p < out->pools.size(); ++p) {
+    for (size_t t = 0; t < out->pools[p].host.size(); ++t) {
+      const void* v = nullptr;
+      st = device_view(out->pools[p].host[t], Want::kAny,
+                       "host tensor " + std::to_string(t) + " of pool " + std::to_string(p), &v);
+      if (st != HICACHE_OK) return st;
+      out->pools[p].host[t] = static_cast<char*>(const_cast<void*>(v));
+    }
+  }
+  const Want w = out->o.index_location == HICACHE_INDEX_HOST ? Want::kHostPinned : Want::kDevice;
+  st = device_view(dev_idx, w, "device_indices", &out->idx.dev_gpu);
+  if (st != HICACHE_OK) return st;
+  st = device_view(host_idx, w, "host_indices", &out->idx.host_gpu);
+  if (st != HICACHE_OK) return st;
+  if (out->o.path == HICACHE_PATH_STAGED &&
+      (!out->o.staging[0] || !out->o.staging[1] || out->o.staging_bytes == 0))
+    return fail(HICACHE_ENOSTAGE, "staged path requested without two staging buffers");
+  return HICACHE_OK;
+}
+
+SideSpec host_side(const std::vector<PoolInfo>& pools) {
+  SideSpec s;
+  s.vec16 = vec16_ok(pools);
+  s.layer_origin = 0;
+  for (const PoolInfo& pi : pools) {
+    s.base.push_back(pi.host);
+    s.layer_stride.push_back(int64_t(pi.P) * pi.token_bytes);
+    s.page_stride.push_back(int64_t(pi.L) * pi.P * pi.token_bytes);
+    s.paged_tokens.push_back(pi.host_pages * pi.P);
+  }
+  return s;
+}
+
+LaunchCfg launch_cfg(const hicache_opts& o) { return LaunchCfg{o.max_ctas, o.device_error}; }
+
+hicache_path resolve_path(const Prepared& pr, Dir dir) {
+  if (pr.o.path != HICACHE_PATH_AUTO) return static_cast<hicache_path>(pr.o.path);
+  return choose_path(pr.pools, pr.o, pr.idx, dir);
+}
+
+void record_events(cudaEvent_t* evs, int32_t count, cudaStream_t stream) {
+  if (!evs) return;
+  for (int32_t i = 0; i < count; ++i)
+    if (evs[i]) cudaEventRecord(evs[i], stream);
+}
+
+hicache_status load_layers(const Prepared& pr, int32_t layer_begin, int32_t layer_end,
+                           cudaStream_t stream, cudaEvent_t* evs) {
+  const int32_t count = layer_end - layer_begin;
+  const hicache_path path = resolve_path(pr, kPagedToDev);
+  if (path == HICACHE_PATH_STAGED)
+    return staged_load(pr.pools, pr.o, pr.idx, layer_begin, layer_end, stream, evs);
+  const SideSpec side = host_side(pr.pools);
+  const LaunchCfg cfg = launch_cfg(pr.o);
+  for (int32_t l = layer_begin; l < layer_end; ++l) {
+    hicache_status st = launch_rows(pr.pools, side, pr.idx.dev_gpu, pr.idx.host_gpu, pr.idx.bits,
+                                    0, pr.idx.n, kPagedToDev, l, l + 1, cfg, stream);
+    if (st != HICACHE_OK) {
+      record_events(evs ? evs + (l - layer_begin) : nullptr, count - (l - layer_begin), stream);
+      return st;
+    }
+    if (evs && evs[l - layer_begin]) {
+      const cudaError_t e = cudaEventRecord(evs[l - layer_begin], stream);
+      if (e != cudaSuccess) {
+        st = cuda_fail(e, "cudaEventRecord(layer_done)");
+        record_events(evs + (l - layer_begin) + 1, count - (l - layer_begin) - 1, stream);
+        return st;
+      }
+    }
+  }
+  return HICACHE_OK;
+}
+
+}  // namespace
+}  // namespace hk
+
+using namespace hk;
+
+extern "C" hicache_status hicache_backup_all_layers(const hicache_pool* pools, int32_t num_pools,
+                                                    const void* device_indices,
+                                                    const void* host_indices, int32_t index_bits,
+                                                    int64_t n, const hicache_opts* opts,
+                                                    cudaStream_t stream) {
+  clear_error();
+  Prepared pr;
+  hicache_status st = prepare(pools, num_pools, device_indices, host_indices, index_bits, n, opts,
+                              /*dest_is_device=*/false, false, 0, 0, &pr);
+  if (st != HICACHE_OK || n == 0) return st;
+  const hicache_path path = resolve_path(pr, kDevToPaged);
+  if (path == HICACHE_PATH_STAGED)
+    return staged_backup(pr.pools, pr.o, pr.idx, stream);
+  return launch_rows(pr.pools, host_side(pr.pools), pr.idx.dev_gpu, pr.idx.host_gpu, pr.idx.bits,
+                     0, pr.idx.n, kDevToPaged, 0, pr.pools[0].L, launch_cfg(pr.o), stream);
+}
+
+extern "C" hicache_status hicache_load_layer(const hicache_pool* pools, int32_t num_pools,
+                                             int32_t layer, const void* host_indices,
+                                             const void* device_indices, int32_t index_bits,
+                                             int64_t n, const hicache_opts* opts,
+                                             cudaStream_t stream, cudaEvent_t layer_done) {
+  clear_error();
+  cudaEvent_t evs[1] = {layer_done};
+  Prepared pr;
+  hicache_status st = prepare(pools, num_pools, device_indices, host_indices, index_bits, n, opts,
+                              /*dest_is_device=*/true, true, layer, layer + 1, &pr);
+  if (st != HICACHE_OK || n == 0) {
+    record_events(evs, 1, stream);
+    return st;
+  }
+  return load_layers(pr, layer, layer + 1, stream, evs);
+}
+
+extern "C" hicache_status hicache_load_burst(const hicache_pool* pools, int32_t num_pools,
+                                             int32_t layer_begin, int32_t layer_end,
+                                             const void* host_indices, const void* device_indices,
+                                             int32_t index_bits, int64_t n,
+                                             const hicache_opts* opts, cudaStream_t stream,
+                                             cudaEvent_t* layer_done) {
+  clear_error();
+  const int32_t count = layer_end > layer_begin ? layer_end - layer_begin : 0;
+  Prepared pr;
+  hicache_status st = prepare(pools, num_pools, device_indices, host_indices, index_bits, n, opts,
+                              /*dest_is_device=*/true, true, layer_begin, layer_end, &pr);
+  if (st != HICACHE_OK || n == 0) {
+    record_events(layer_done, count, stream);
+    return st;
+  }
+  return load_layers(pr, layer_begin, layer_end, stream, layer_done);
+}
+
+extern "C" hicache_status hicache_plan_runs(const void* device_indices, const void* host_indices,
+                                            int32_t index_bits, int64_t n, int32_t page_size,
+                                            hicache_run* runs_out, int64_t runs_cap,
+                                            int64_t* num_runs, int64_t* full_pages) {
+  clear_error();
+  hicache_status st = check_index_args(device_indices, host_indices, index_bits, n);
+  if (st != HICACHE_OK) return st;
+  return plan_runs(device_indices, host_indices, index_bits, n, page_size, runs_out, runs_cap,
+                   num_runs, full_pages);
+}
+
+extern "C" hicache_status hicache_layer_checksum(const hicache_pool* pool, int32_t tensor,
+                                                 int32_t layer, const void* device_indices,
+                                                 int32_t index_bits, int64_t n, uint64_t* out_sum,
+                                                 cudaStream_t stream) {
+  clear_error();
+  std::vector<PoolInfo> pools;
+  hicache_status st = check_pools(pool, 1, &pools);
+  if (st != HICACHE_OK) return st;
+  st = check_index_args(device_indices, device_indices, index_bits, n);
+  if (st != HICACHE_OK) return st;
+  if (tensor < 0 || tensor >= pools[0].T) return fail(HICACHE_EINVAL, "tensor out of range");
+  if (layer < 0 || layer >= pools[0].L) return fail(HICACHE_EINVAL, "layer out of range");
+  if (!out_sum) return fail(HICACHE_EINVAL, "out_sum is NULL");
+  if (n == 0) return HICACHE_OK;
+  const void* v = nullptr;
+  st = device_view(device_indices, Want::kDevice, "device_indices", &v);
+  if (st != HICACHE_OK) return st;
+  return launch_checksum(pools[0], tensor, layer, v, index_bits, n, out_sum, stream);
+}
+
+extern "C" int64_t hicache_kernel_launches(void) { return kernel_launches(); }
+
+extern "C" const char* hicache_last_error(void) { return last_error().c_str(); }
+
+extern "C" int32_t hicache_abi_version(void) { return HICACHE_ABI_VERSION; }

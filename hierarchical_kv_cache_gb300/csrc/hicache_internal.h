@@ -1,0 +1,144 @@
+// hicache_internal.h -- types shared by the library's translation units.
+//
+// Nothing here is part of the public ABI (include/hicache.h is).  The copy
+// kernels see a transfer as a list of "segments": one segment is the stream of
+// rows of one (pool, tensor, layer) between a layer-first device buffer and the
+// page-first host tensor (or an HBM staging buffer laid out like it).
+#pragma once
+
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include <cuda_runtime_api.h>
+
+#include "hicache.h"
+
+namespace hk {
+
+constexpr int kMaxPools = 4;
+constexpr int kWarpsPerCta = 8;     // 256-thread CTAs
+constexpr int kThreadsPerCta = kWarpsPerCta * 32;
+constexpr int kUnroll = 4;          // 16-byte chunks in flight per lane per iteration
+constexpr int kMaxSegSmall = 8;     // per-layer launches: pools x tensors
+constexpr int kMaxSegLarge = 512;   // all-layer launches: pools x tensors x layers
+
+// Direction of one launch.
+enum Dir : int32_t { kDevToPaged = 0, kPagedToDev = 1 };
+
+// Row geometry of one pool for one launch.  A "row" is what one pair moves:
+// a token row (R bytes) for token pools, a whole page row (P * R bytes) for
+// page-granular pools.
+struct PoolGeom {
+  int64_t row_bytes;         // bytes moved per row
+  int64_t paged_page_stride; // bytes from one page of the paged side to the next
+  int64_t dev_tokens;        // token rows of one device layer buffer (range check)
+  int64_t paged_tokens;      // token rows of the paged side (range check)
+  int64_t nrows;             // rows moved by one segment of this pool
+  int64_t tasks_per_seg;     // ceil(nrows / rows_per_task)
+  int32_t rows_per_page;     // P for token pools, 1 for page-granular pools
+  int32_t idx_stride;        // pair index of row k is k * idx_stride (P for page pools)
+  int32_t idx_div;           // token index -> row index divisor (P for page pools)
+  int32_t rows_per_task;     // 1..32 rows handled by one warp task
+  uint32_t cpr;              // chunks (VEC bytes) per row
+  uint32_t q32, r32;         // 32 == q32 * cpr + r32
+  uint32_t qS, rS;           // 32 * kUnroll == qS * cpr + rS
+  uint32_t pad;
+};
+
+// One (pool, tensor, layer) stream.
+struct Segment {
+  char* dev;    // device layer buffer base
+  char* paged;  // paged-side base of this layer: host tensor (or staging) + layer block offset
+  int32_t pool;
+  int32_t pad;
+};
+
+template <int MAXSEG>
+struct CopyParams {
+  const void* dev_idx;      // device-slot indices (device-accessible)
+  const void* paged_idx;    // paged-side token indices; NULL = pair index - pair_begin
+  uint32_t* err;            // optional device-accessible error word
+  int64_t pair_begin;       // first pair moved by this launch
+  int32_t nseg;
+  int32_t dir;              // Dir
+  PoolGeom pool[kMaxPools];
+  int64_t seg_task_begin[MAXSEG + 1];
+  Segment seg[MAXSEG];
+};
+
+// Host-side description of one validated pool.
+struct PoolInfo {
+  int32_t L, T, P;
+  int32_t page_granular;
+  int64_t token_bytes;      // R of one token row
+  int64_t device_slots, host_pages;
+  std::vector<char*> dev;   // T * L device layer pointers
+  std::vector<char*> host;  // T host tensor pointers (device-visible addresses)
+};
+
+// The two index arrays of a call: addresses the kernels use and, for host-located
+// indices, addresses the CPU reads (NULL for device-located indices).
+struct IndexSet {
+  const void* dev_gpu = nullptr;
+  const void* host_gpu = nullptr;
+  const void* dev_cpu = nullptr;
+  const void* host_cpu = nullptr;
+  int32_t bits = 64;
+  int64_t n = 0;
+};
+
+// Per-thread last error message.
+void set_error(const std::string& msg);
+void clear_error();
+hicache_status fail(hicache_status st, const std::string& msg);
+
+// Validation helpers (validate.cpp).
+hicache_status check_pools(const hicache_pool* pools, int32_t num_pools, std::vector<PoolInfo>* out);
+hicache_status check_index_args(const void* a, const void* b, int32_t index_bits, int64_t n);
+// Range, distinct destinations and page-granular whole pages, on host-readable indices.
+// dest_is_device selects which side must be distinct.
+hicache_status check_pairs_host(const std::vector<PoolInfo>& pools, const void* dev_idx,
+                                const void* host_idx, int32_t index_bits, int64_t n,
+                                bool dest_is_device);
+hicache_status plan_runs(const void* dev_idx, const void* host_idx, int32_t index_bits, int64_t n,
+                         int32_t page_size, hicache_run* runs, int64_t cap, int64_t* num_runs,
+                         int64_t* full_pages);
+
+// Launch-side helpers (zero_copy.cu).
+constexpr int kDefaultCtasPerSm = 2;
+
+struct LaunchCfg {
+  int max_ctas;   // 0 = default
+  uint32_t* err;
+};
+
+// The page-first side of a launch: the pinned host pool, or an HBM staging
+// buffer laid out the same way.  Indexed [pool] and [pool][tensor].
+struct SideSpec {
+  bool vec16 = false;                     // 16-byte chunks usable on both sides
+  int32_t layer_origin = 0;               // layer whose block starts at base
+  std::vector<std::vector<char*>> base;   // [pool][tensor] base address
+  std::vector<int64_t> layer_stride;      // [pool] bytes between layer blocks of one page
+  std::vector<int64_t> page_stride;       // [pool] bytes between pages
+  std::vector<int64_t> paged_tokens;      // [pool] token rows addressable on this side
+};
+
+int64_t moved_row_bytes(const PoolInfo& pi);
+bool vec16_ok(const std::vector<PoolInfo>& pools);
+void fill_geometry(const PoolInfo& pi, int64_t npairs, int vec, int64_t paged_page_stride,
+                   int64_t paged_tokens, PoolGeom* g);
+// Moves pairs [pair_begin, pair_begin + npairs) for layers [layer_begin, layer_end)
+// of every pool and tensor between the device buffers and `side`.
+hicache_status launch_rows(const std::vector<PoolInfo>& pools, const SideSpec& side,
+                           const void* dev_idx, const void* paged_idx, int32_t index_bits,
+                           int64_t pair_begin, int64_t npairs, Dir dir, int32_t layer_begin,
+                           int32_t layer_end, const LaunchCfg& cfg, cudaStream_t stream);
+hicache_status launch_checksum(const PoolInfo& pool, int32_t tensor, int32_t layer,
+                               const void* dev_idx, int32_t index_bits, int64_t n,
+                               uint64_t* out, cudaStream_t stream);
+int device_sm_count();
+void count_launch();
+int64_t kernel_launches();
+
+}  // namespace hk

@@ -1,0 +1,281 @@
+// staged.cu -- transfers through an HBM staging buffer plus copy-engine DMA.
+//
+// Prior art: the staged write-back of "[HiCache] Support hybrid-pool staged
+// write-back JIT kernel" (sglang PR #28434 summary) packs device rows into a
+// page-first staging buffer of a fixed number of pages and then copies it to
+// the host.  Here the staging is double-buffered so that the gather of chunk
+// k+1 overlaps the link transfer of chunk k, the DMA is one copy per run of
+// consecutive host pages (not one per row), and the same idea serves the
+// per-layer load in reverse (2-D DMA of one layer block per host page, then a
+// scatter kernel).  The staged path needs the pairs to be whole host pages in
+// groups of page_size (what a page-granular host allocator hands out) and the
+// indices on the host, because the DMA spans are planned on the CPU.
+#include <cuda_runtime.h>
+
+#include <string>
+#include <vector>
+
+#include "staged.h"
+
+namespace hk {
+
+namespace {
+
+hicache_status cuda_fail(cudaError_t e, const std::string& what) {
+  return fail(HICACHE_ECUDA, what + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")");
+}
+
+#define HK_CUDA(call, what)                       \
+  do {                                            \
+    const cudaError_t e_ = (call);                \
+    if (e_ != cudaSuccess) return cuda_fail(e_, what); \
+  } while (0)
+
+// Events and the internal copy stream, created once per thread and device.
+struct StagedRes {
+  bool init = false;
+  cudaStream_t copy = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  cudaEvent_t ready[2] = {nullptr, nullptr};
+  cudaEvent_t freed[2] = {nullptr, nullptr};
+};
+
+hicache_status get_res(StagedRes** out) {
+  static thread_local StagedRes res[64];
+  int dev = 0;
+  HK_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(HICACHE_EINVAL, "device ordinal above 63");
+  StagedRes& r = res[dev];
+  if (!r.init) {
+    HK_CUDA(cudaStreamCreateWithFlags(&r.copy, cudaStreamNonBlocking), "cudaStreamCreate(copy)");
+    cudaEvent_t* evs[6] = {&r.fork, &r.join, &r.ready[0], &r.ready[1], &r.freed[0], &r.freed[1]};
+    for (cudaEvent_t* e : evs) HK_CUDA(cudaEventCreateWithFlags(e, cudaEventDisableTiming), "cudaEventCreate");
+    r.init = true;
+  }
+  *out = &r;
+  return HICACHE_OK;
+}
+
+bool aligned16(const void* p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; }
+
+// Staging layout: one region per (pool, tensor), each `cap_pages` pages of
+// `page_bytes(pool)` bytes; region offsets are in (pool, tensor) order.
+struct StagingLayout {
+  int64_t cap_pages = 0;
+  std::vector<std::vector<int64_t>> region_off;  // [pool][tensor]
+  bool vec16 = false;
+};
+
+StagingLayout layout_for(const std::vector<PoolInfo>& pools, const hicache_opts& o,
+                         bool all_layers) {
+  StagingLayout s;
+  int64_t per_page = 0;
+  for (const PoolInfo& pi : pools)
+    per_page += int64_t(pi.T) * (all_layers ? pi.L : 1) * pi.P * pi.token_bytes;
+  s.cap_pages = per_page > 0 ? int64_t(o.staging_bytes) / per_page : 0;
+  int64_t off = 0;
+  s.vec16 = vec16_ok(pools) && aligned16(o.staging[0]) && aligned16(o.staging[1]);
+  for (const PoolInfo& pi : pools) {
+    std::vector<int64_t> offs;
+    const int64_t region = s.cap_pages * (all_layers ? pi.L : 1) * pi.P * pi.token_bytes;
+    for (int32_t t = 0; t < pi.T; ++t) {
+      offs.push_back(off);
+      if (off % 16 != 0) s.vec16 = false;
+      off += region;
+    }
+    s.region_off.push_back(offs);
+  }
+  return s;
+}
+
+SideSpec staging_side(const std::vector<PoolInfo>& pools, const StagingLayout& lay, char* base,
+                      bool all_layers, int32_t layer_origin) {
+  SideSpec side;
+  side.vec16 = lay.vec16;
+  side.layer_origin = layer_origin;
+  for (size_t p = 0; p < pools.size(); ++p) {
+    const PoolInfo& pi = pools[p];
+    std::vector<char*> b;
+    for (int32_t t = 0; t < pi.T; ++t) b.push_back(base + lay.region_off[p][size_t(t)]);
+    side.base.push_back(b);
+    const int64_t block = int64_t(pi.P) * pi.token_bytes;  // one (page, layer) block
+    side.layer_stride.push_back(all_layers ? block : 0);
+    side.page_stride.push_back(all_layers ? block * pi.L : block);
+    side.paged_tokens.push_back(lay.cap_pages * pi.P);
+  }
+  return side;
+}
+
+template <typename T>
+int64_t at(const void* p, int64_t i) {
+  return int64_t(static_cast<const T*>(p)[i]);
+}
+
+hicache_status need_pages(const IndexSet& idx, int32_t P, std::vector<int64_t>* pages) {
+  if (!idx.host_cpu)
+    return fail(HICACHE_EINVAL, "staged path needs host-located indices (the DMA spans are planned on the CPU)");
+  if (!host_page_groups(idx.host_cpu, idx.bits, idx.n, P, pages))
+    return fail(HICACHE_EINVAL, "staged path needs the pairs to be whole host pages in groups of page_size");
+  return HICACHE_OK;
+}
+
+}  // namespace
+
+bool host_page_groups(const void* host_idx, int32_t bits, int64_t n, int32_t page_size,
+                      std::vector<int64_t>* pages) {
+  const int64_t P = page_size;
+  if (n % P != 0) return false;
+  pages->clear();
+  pages->reserve(size_t(n / P));
+  for (int64_t k = 0; k < n; k += P) {
+    const int64_t h0 = bits == 32 ? at<int32_t>(host_idx, k) : at<int64_t>(host_idx, k);
+    if (h0 % P != 0) return false;
+    for (int64_t t = 1; t < P; ++t) {
+      const int64_t h = bits == 32 ? at<int32_t>(host_idx, k + t) : at<int64_t>(host_idx, k + t);
+      if (h != h0 + t) return false;
+    }
+    pages->push_back(h0 / P);
+  }
+  return true;
+}
+
+hicache_status staged_backup(const std::vector<PoolInfo>& pools, const hicache_opts& o,
+                             const IndexSet& idx, cudaStream_t stream) {
+  const int32_t P = pools[0].P;
+  const int32_t L = pools[0].L;
+  std::vector<int64_t> hp;
+  hicache_status st = need_pages(idx, P, &hp);
+  if (st != HICACHE_OK) return st;
+  const StagingLayout lay = layout_for(pools, o, /*all_layers=*/true);
+  if (lay.cap_pages < 1)
+    return fail(HICACHE_ENOSTAGE, "staging buffers hold less than one host page of all layers");
+  StagedRes* r = nullptr;
+  st = get_res(&r);
+  if (st != HICACHE_OK) return st;
+  cudaStream_t copy = o.copy_stream ? o.copy_stream : r->copy;
+  const LaunchCfg cfg{o.max_ctas, o.device_error};
+  const int64_t groups = int64_t(hp.size());
+  const SideSpec side[2] = {staging_side(pools, lay, static_cast<char*>(o.staging[0]), true, 0),
+                            staging_side(pools, lay, static_cast<char*>(o.staging[1]), true, 0)};
+
+  HK_CUDA(cudaEventRecord(r->fork, stream), "cudaEventRecord(fork)");
+  HK_CUDA(cudaStreamWaitEvent(copy, r->fork, 0), "cudaStreamWaitEvent(fork)");
+  for (int64_t k = 0, g0 = 0; g0 < groups; ++k, g0 += lay.cap_pages) {
+    const int b = int(k & 1);
+    const int64_t g1 = std::min(groups, g0 + lay.cap_pages);
+    // the DMA of chunk k-2 must have drained buffer b before the gather reuses it
+    if (k >= 2) HK_CUDA(cudaStreamWaitEvent(stream, r->freed[b], 0), "cudaStreamWaitEvent(freed)");
+    st = launch_rows(pools, side[b], idx.dev_gpu, nullptr, idx.bits, g0 * P, (g1 - g0) * P,
+                     kDevToPaged, 0, L, cfg, stream);
+    if (st != HICACHE_OK) return st;
+    HK_CUDA(cudaEventRecord(r->ready[b], stream), "cudaEventRecord(ready)");
+    HK_CUDA(cudaStreamWaitEvent(copy, r->ready[b], 0), "cudaStreamWaitEvent(ready)");
+    for (size_t p = 0; p < pools.size(); ++p) {
+      const PoolInfo& pi = pools[p];
+      const int64_t page_bytes = int64_t(L) * pi.P * pi.token_bytes;  // one host page, all layers
+      for (int32_t t = 0; t < pi.T; ++t) {
+        for (int64_t j = g0; j < g1;) {
+          int64_t e = j + 1;
+          while (e < g1 && hp[size_t(e)] == hp[size_t(e - 1)] + 1) ++e;
+          char* dst = pi.host[size_t(t)] + hp[size_t(j)] * page_bytes;
+          const char* src = side[b].base[p][size_t(t)] + (j - g0) * page_bytes;
+          HK_CUDA(cudaMemcpyAsync(dst, src, size_t((e - j) * page_bytes), cudaMemcpyDeviceToHost, copy),
+                  "cudaMemcpyAsync(staging -> host)");
+          j = e;
+        }
+      }
+    }
+    HK_CUDA(cudaEventRecord(r->freed[b], copy), "cudaEventRecord(freed)");
+  }
+  HK_CUDA(cudaEventRecord(r->join, copy), "cudaEventRecord(join)");
+  HK_CUDA(cudaStreamWaitEvent(stream, r->join, 0), "cudaStreamWaitEvent(join)");
+  return HICACHE_OK;
+}
+
+hicache_status staged_load(const std::vector<PoolInfo>& pools, const hicache_opts& o,
+                           const IndexSet& idx, int32_t layer_begin, int32_t layer_end,
+                           cudaStream_t stream, cudaEvent_t* layer_done) {
+  const int32_t P = pools[0].P;
+  const int32_t L = pools[0].L;
+  const int32_t count = layer_end - layer_begin;
+  auto finish = [&](int32_t from, hicache_status s) {
+    // a failed load still completes every remaining layer event
+    for (int32_t i = from; i < count; ++i)
+      if (layer_done && layer_done[i]) cudaEventRecord(layer_done[i], stream);
+    return s;
+  };
+  std::vector<int64_t> hp;
+  hicache_status st = need_pages(idx, P, &hp);
+  if (st != HICACHE_OK) return finish(0, st);
+  const StagingLayout lay = layout_for(pools, o, /*all_layers=*/false);
+  if (lay.cap_pages < 1)
+    return finish(0, fail(HICACHE_ENOSTAGE, "staging buffers hold less than one host page of one layer"));
+  StagedRes* r = nullptr;
+  st = get_res(&r);
+  if (st != HICACHE_OK) return finish(0, st);
+  cudaStream_t copy = o.copy_stream ? o.copy_stream : r->copy;
+  const LaunchCfg cfg{o.max_ctas, o.device_error};
+  const int64_t groups = int64_t(hp.size());
+
+#define HK_TRY(call, what)                                    \
+  do {                                                        \
+    const cudaError_t e_ = (call);                            \
+    if (e_ != cudaSuccess) return finish(l - layer_begin, cuda_fail(e_, what)); \
+  } while (0)
+
+  int32_t l = layer_begin;
+  HK_TRY(cudaEventRecord(r->fork, stream), "cudaEventRecord(fork)");
+  HK_TRY(cudaStreamWaitEvent(copy, r->fork, 0), "cudaStreamWaitEvent(fork)");
+  int64_t step = 0;
+  for (; l < layer_end; ++l) {
+    for (int64_t g0 = 0; g0 < groups; g0 += lay.cap_pages, ++step) {
+      const int b = int(step & 1);
+      const int64_t g1 = std::min(groups, g0 + lay.cap_pages);
+      const SideSpec side = staging_side(pools, lay, static_cast<char*>(o.staging[b]), false, l);
+      // the scatter of step-2 must have read buffer b before the DMA refills it
+      if (step >= 2) HK_TRY(cudaStreamWaitEvent(copy, r->freed[b], 0), "cudaStreamWaitEvent(freed)");
+      for (size_t p = 0; p < pools.size(); ++p) {
+        const PoolInfo& pi = pools[p];
+        const int64_t block = int64_t(pi.P) * pi.token_bytes;  // one (page, layer) block
+        const int64_t host_page = block * L;
+        for (int32_t t = 0; t < pi.T; ++t) {
+          for (int64_t j = g0; j < g1;) {
+            int64_t e = j + 1;
+            while (e < g1 && hp[size_t(e)] == hp[size_t(e - 1)] + 1) ++e;
+            const char* src = pi.host[size_t(t)] + hp[size_t(j)] * host_page + int64_t(l) * block;
+            char* dst = side.base[p][size_t(t)] + (j - g0) * block;
+            HK_TRY(cudaMemcpy2DAsync(dst, size_t(block), src, size_t(host_page), size_t(block),
+                                     size_t(e - j), cudaMemcpyHostToDevice, copy),
+                   "cudaMemcpy2DAsync(host -> staging)");
+            j = e;
+          }
+        }
+      }
+      HK_TRY(cudaEventRecord(r->ready[b], copy), "cudaEventRecord(ready)");
+      HK_TRY(cudaStreamWaitEvent(stream, r->ready[b], 0), "cudaStreamWaitEvent(ready)");
+      st = launch_rows(pools, side, idx.dev_gpu, nullptr, idx.bits, g0 * P, (g1 - g0) * P,
+                       kPagedToDev, l, l + 1, cfg, stream);
+      if (st != HICACHE_OK) return finish(l - layer_begin, st);
+      HK_TRY(cudaEventRecord(r->freed[b], stream), "cudaEventRecord(freed)");
+    }
+    if (layer_done && layer_done[l - layer_begin])
+      HK_TRY(cudaEventRecord(layer_done[l - layer_begin], stream), "cudaEventRecord(layer_done)");
+  }
+#undef HK_TRY
+  return HICACHE_OK;
+}
+
+hicache_path choose_path(const std::vector<PoolInfo>& pools, const hicache_opts& o,
+                         const IndexSet& idx, Dir dir) {
+  (void)pools;
+  (void)idx;
+  (void)dir;
+  // The staged path needs host-located indices and two staging buffers; on the
+  // measured host link the zero-copy kernels reach the DMA bandwidth, so the
+  // zero-copy path is the default whenever it applies.
+  if (!o.staging[0] || !o.staging[1] || o.staging_bytes == 0 || !idx.host_cpu)
+    return HICACHE_PATH_ZERO_COPY;
+  return HICACHE_PATH_ZERO_COPY;
+}
+
+}  // namespace hk

@@ -1,0 +1,225 @@
+// validate.cpp -- host-side argument checks and the run planner.
+//
+// Everything here is plain C++ and calls no CUDA function, so it runs (and is
+// tested) on machines without a GPU.  Index validation replaces the per-chunk
+// copy-descriptor build that the per-layer load performs on the CPU in the
+// HiCache pages ("[HiCache] Run the host->device load-back enqueue on a loader
+// thread", Motivation): one O(n) pass per call or per burst, then nothing per
+// layer.
+#include <algorithm>
+#include <cstring>
+#include <limits>
+#include <string>
+#include <vector>
+
+#include "hicache_internal.h"
+
+namespace hk {
+
+namespace {
+thread_local std::string g_last_error;
+
+template <typename T>
+inline int64_t idx_at(const void* p, int64_t i) {
+  return static_cast<int64_t>(static_cast<const T*>(p)[i]);
+}
+
+inline int64_t idx(const void* p, int32_t bits, int64_t i) {
+  return bits == 32 ? idx_at<int32_t>(p, i) : idx_at<int64_t>(p, i);
+}
+
+std::string str(int64_t v) { return std::to_string(v); }
+
+constexpr int64_t kMaxRows = (int64_t(1) << 31) - 1;
+}  // namespace
+
+hicache_status check_whole_pages(bool any_page, int64_t P, const void* dev_idx, const void* host_idx,
+                                 int32_t bits, int64_t n);
+
+void set_error(const std::string& msg) { g_last_error = msg; }
+void clear_error() { g_last_error.clear(); }
+hicache_status fail(hicache_status st, const std::string& msg) {
+  set_error(msg);
+  return st;
+}
+const std::string& last_error() { return g_last_error; }
+
+hicache_status check_pools(const hicache_pool* pools, int32_t num_pools, std::vector<PoolInfo>* out) {
+  if (!pools) return fail(HICACHE_EINVAL, "pools is NULL");
+  if (num_pools < 1 || num_pools > kMaxPools)
+    return fail(HICACHE_EINVAL, "num_pools must be in 1.." + str(kMaxPools));
+  out->clear();
+  for (int32_t p = 0; p < num_pools; ++p) {
+    const hicache_pool& q = pools[p];
+    const std::string who = "pool " + str(p) + ": ";
+    if (q.num_layers < 1 || q.num_layers > 4096) return fail(HICACHE_EINVAL, who + "num_layers must be in 1..4096");
+    if (q.num_tensors < 1 || q.num_tensors > 2) return fail(HICACHE_EINVAL, who + "num_tensors must be 1 or 2");
+    if (q.head_num < 1 || q.head_dim < 1 || q.dtype_size < 1)
+      return fail(HICACHE_EINVAL, who + "head_num, head_dim and dtype_size must be positive");
+    if (q.page_size < 1) return fail(HICACHE_EINVAL, who + "page_size must be positive");
+    if (q.page_granular != 0 && q.page_granular != 1) return fail(HICACHE_EINVAL, who + "page_granular must be 0 or 1");
+    if (q.reserved != 0) return fail(HICACHE_EINVAL, who + "reserved must be 0");
+    const int64_t R = int64_t(q.head_num) * q.head_dim * q.dtype_size;
+    if (R > (int64_t(1) << 24)) return fail(HICACHE_EINVAL, who + "row bytes above 16 MiB");
+    if (R % 4 != 0) return fail(HICACHE_EALIGN, who + "row bytes " + str(R) + " not a multiple of 4");
+    if (q.device_slots < 0 || q.host_pages < 0) return fail(HICACHE_EINVAL, who + "negative pool size");
+    if (q.device_slots > kMaxRows || q.host_pages * int64_t(q.page_size) > kMaxRows)
+      return fail(HICACHE_EINVAL, who + "pool holds more than 2^31-1 token rows");
+    if (q.page_granular && q.device_slots % q.page_size != 0)
+      return fail(HICACHE_EINVAL, who + "page-granular pool: device_slots not a multiple of page_size");
+    if (q.page_granular && int64_t(q.page_size) * R > (int64_t(1) << 24))
+      return fail(HICACHE_EINVAL, who + "page row above 16 MiB");
+    if (!q.device_layers || !q.host_tensors) return fail(HICACHE_EINVAL, who + "NULL pointer table");
+    PoolInfo pi;
+    pi.L = q.num_layers;
+    pi.T = q.num_tensors;
+    pi.P = q.page_size;
+    pi.page_granular = q.page_granular;
+    pi.token_bytes = R;
+    pi.device_slots = q.device_slots;
+    pi.host_pages = q.host_pages;
+    pi.dev.resize(size_t(pi.T) * pi.L);
+    pi.host.resize(size_t(pi.T));
+    for (int32_t i = 0; i < pi.T * pi.L; ++i) {
+      char* ptr = static_cast<char*>(q.device_layers[i]);
+      if (!ptr) return fail(HICACHE_EINVAL, who + "device layer pointer " + str(i) + " is NULL");
+      if (reinterpret_cast<uintptr_t>(ptr) % 4 != 0)
+        return fail(HICACHE_EALIGN, who + "device layer pointer " + str(i) + " not 4-byte aligned");
+      pi.dev[size_t(i)] = ptr;
+    }
+    for (int32_t t = 0; t < pi.T; ++t) {
+      char* ptr = static_cast<char*>(q.host_tensors[t]);
+      if (!ptr) return fail(HICACHE_EINVAL, who + "host tensor pointer " + str(t) + " is NULL");
+      if (reinterpret_cast<uintptr_t>(ptr) % 4 != 0)
+        return fail(HICACHE_EALIGN, who + "host tensor pointer " + str(t) + " not 4-byte aligned");
+      pi.host[size_t(t)] = ptr;
+    }
+    out->push_back(std::move(pi));
+  }
+  for (size_t p = 1; p < out->size(); ++p) {
+    if ((*out)[p].L != (*out)[0].L)
+      return fail(HICACHE_EINVAL, "pools of one call must have the same num_layers");
+    if ((*out)[p].P != (*out)[0].P)
+      return fail(HICACHE_EINVAL, "pools of one call must have the same page_size");
+  }
+  return HICACHE_OK;
+}
+
+hicache_status check_index_args(const void* a, const void* b, int32_t index_bits, int64_t n) {
+  if (index_bits != 32 && index_bits != 64) return fail(HICACHE_EINVAL, "index_bits must be 32 or 64");
+  if (n < 0) return fail(HICACHE_EINVAL, "n is negative");
+  if (n > kMaxRows) return fail(HICACHE_EINVAL, "n above 2^31-1");
+  if (n > 0 && (!a || !b)) return fail(HICACHE_EINVAL, "NULL index array");
+  return HICACHE_OK;
+}
+
+hicache_status check_pairs_host(const std::vector<PoolInfo>& pools, const void* dev_idx,
+                                const void* host_idx, int32_t bits, int64_t n, bool dest_is_device) {
+  if (n == 0) return HICACHE_OK;
+  int64_t dev_lim = std::numeric_limits<int64_t>::max();
+  int64_t host_lim = std::numeric_limits<int64_t>::max();
+  bool any_page = false;
+  const int64_t P = pools[0].P;
+  for (const PoolInfo& p : pools) {
+    dev_lim = std::min(dev_lim, p.device_slots);
+    host_lim = std::min(host_lim, p.host_pages * int64_t(p.P));
+    any_page = any_page || p.page_granular;
+  }
+  // Range: every pair must address a row of every pool of the call.
+  for (int64_t i = 0; i < n; ++i) {
+    const int64_t d = idx(dev_idx, bits, i);
+    const int64_t h = idx(host_idx, bits, i);
+    if (d < 0 || d >= dev_lim)
+      return fail(HICACHE_ERANGE, "device index " + str(d) + " at pair " + str(i) + " outside [0, " + str(dev_lim) + ")");
+    if (h < 0 || h >= host_lim)
+      return fail(HICACHE_ERANGE, "host index " + str(h) + " at pair " + str(i) + " outside [0, " + str(host_lim) + ")");
+  }
+  // Distinct destinations: a bitmap over the destination rows, cleared again
+  // after use so that the cost stays O(n) per call.
+  const void* dst = dest_is_device ? dev_idx : host_idx;
+  const int64_t lim = dest_is_device ? dev_lim : host_lim;
+  if (lim > (int64_t(1) << 28) && lim / 64 > 4 * n) {
+    // Sparse use of a huge destination space: sort a copy instead of a bitmap.
+    std::vector<int64_t> v(static_cast<size_t>(n));
+    for (int64_t i = 0; i < n; ++i) v[size_t(i)] = idx(dst, bits, i);
+    std::sort(v.begin(), v.end());
+    for (size_t i = 1; i < v.size(); ++i)
+      if (v[i] == v[i - 1])
+        return fail(HICACHE_EDUP, std::string(dest_is_device ? "device" : "host") + " destination " +
+                                      str(v[i]) + " named twice");
+    return check_whole_pages(any_page, P, dev_idx, host_idx, bits, n);
+  }
+  static thread_local std::vector<uint64_t> bitmap;
+  const size_t words = size_t((lim + 63) / 64);
+  if (bitmap.size() < words) bitmap.assign(words, 0);
+  hicache_status st = HICACHE_OK;
+  int64_t set_upto = n;
+  for (int64_t i = 0; i < n; ++i) {
+    const int64_t x = idx(dst, bits, i);
+    uint64_t& w = bitmap[size_t(x >> 6)];
+    const uint64_t bit = uint64_t(1) << (x & 63);
+    if (w & bit) {
+      st = fail(HICACHE_EDUP, std::string(dest_is_device ? "device" : "host") + " destination " + str(x) +
+                                  " named twice (second time at pair " + str(i) + ")");
+      set_upto = i;
+      break;
+    }
+    w |= bit;
+  }
+  for (int64_t i = 0; i < set_upto; ++i) bitmap[size_t(idx(dst, bits, i) >> 6)] = 0;
+  if (st != HICACHE_OK) return st;
+  return check_whole_pages(any_page, P, dev_idx, host_idx, bits, n);
+}
+
+hicache_status check_whole_pages(bool any_page, int64_t P, const void* dev_idx, const void* host_idx,
+                                 int32_t bits, int64_t n) {
+  // Page-granular pools move whole aligned pages.
+  if (any_page) {
+    if (n % P != 0)
+      return fail(HICACHE_EINVAL, "page-granular pool: n=" + str(n) + " is not a multiple of page_size " + str(P));
+    for (int64_t k = 0; k < n; k += P) {
+      const int64_t d0 = idx(dev_idx, bits, k);
+      const int64_t h0 = idx(host_idx, bits, k);
+      if (d0 % P != 0 || h0 % P != 0)
+        return fail(HICACHE_EINVAL, "page-granular pool: pair " + str(k) + " does not start a page");
+      for (int64_t t = 1; t < P; ++t) {
+        if (idx(dev_idx, bits, k + t) != d0 + t || idx(host_idx, bits, k + t) != h0 + t)
+          return fail(HICACHE_EINVAL, "page-granular pool: pairs " + str(k) + ".." + str(k + P - 1) +
+                                          " are not one whole page");
+      }
+    }
+  }
+  return HICACHE_OK;
+}
+
+hicache_status plan_runs(const void* dev_idx, const void* host_idx, int32_t bits, int64_t n,
+                         int32_t page_size, hicache_run* runs, int64_t cap, int64_t* num_runs,
+                         int64_t* full_pages) {
+  if (page_size < 1) return fail(HICACHE_EINVAL, "page_size must be positive");
+  if (!num_runs) return fail(HICACHE_EINVAL, "num_runs is NULL");
+  if (cap < 0) return fail(HICACHE_EINVAL, "runs_cap is negative");
+  const int64_t P = page_size;
+  int64_t count = 0, full = 0;
+  int64_t i = 0;
+  while (i < n) {
+    const int64_t d0 = idx(dev_idx, bits, i);
+    const int64_t h0 = idx(host_idx, bits, i);
+    int64_t len = 1;
+    // extend while both sides step by one and the host side stays in its page
+    while (i + len < n) {
+      const int64_t d = idx(dev_idx, bits, i + len);
+      const int64_t h = idx(host_idx, bits, i + len);
+      if (d != d0 + len || h != h0 + len || h % P == 0) break;
+      ++len;
+    }
+    if (runs && count < cap) runs[count] = hicache_run{d0, h0, len};
+    if (len == P && h0 % P == 0) ++full;
+    ++count;
+    i += len;
+  }
+  *num_runs = count;
+  if (full_pages) *full_pages = full;
+  return HICACHE_OK;
+}
+
+}  // namespace hk

@@ -1,0 +1,225 @@
+/*
+ * hicache.h -- C ABI of the GB300 paged KV-cache transfer library.
+ *
+ * The library moves token rows between a layer-first device KV pool (HBM) and
+ * a page-first pinned host pool, driven by lists of (device slot, host slot)
+ * pairs.  Two operations exist:
+ *
+ *   - the all-layer backup (device -> host write-back), and
+ *   - the per-layer load-back (host -> device), one layer per call or a burst
+ *     of layers with one completion event per layer, so that a consumer can
+ *     start on layer l while layer l+1 is still being copied.
+ *
+ * Passages that define the operations:
+ *   - "[HiCache] Support hybrid-pool staged write-back JIT kernel" (sglang PR
+ *     #28434 summary), key source excerpts: backup_from_device_all_layer of the
+ *     MHA host pool and the CPU simulation of the staged lf->pf copy (for every
+ *     layer, the host rows named by the destination indices take the device rows
+ *     named by the source indices).
+ *   - "[HiCache] Run the host->device load-back enqueue on a loader thread"
+ *     (sglang PR #38472), Motivation: per-layer load_to_device_per_layer with the
+ *     page_first_direct host layout and LayerDoneCounter.wait_until in the
+ *     attention layers; Modifications: a failed load still completes every layer
+ *     event so that a waiting consumer cannot hang.
+ *
+ * Layouts (all data are opaque bytes; no arithmetic is done on values):
+ *   R = head_num * head_dim * dtype_size bytes per token row of one tensor.
+ *   Device: tensor t, layer l is one buffer of device_slots rows; slot d starts
+ *           at byte d * R of device_layers[t * num_layers + l].
+ *   Host:   tensor t is one buffer, page-first: host token h of layer l starts at
+ *           byte ((h / P) * num_layers + l) * P * R + (h % P) * R of
+ *           host_tensors[t].  One (page, layer) block is P * R contiguous bytes
+ *           and one page holds the blocks of all layers in layer order.
+ *   A page-granular pool (DSA indexer-K: 128 fp8 values + one 4-byte scale per
+ *   token) uses the same formulas; it only requires that the pairs cover whole,
+ *   page-aligned pages, so that the library may move one P * R page row at a
+ *   time even when R is not a multiple of 16.
+ *
+ * Ownership and ordering:
+ *   The caller owns every pool, index array, staging buffer, stream and event;
+ *   the library allocates no device or pinned memory on any call.  All work is
+ *   stream-ordered on `stream`: it starts after everything enqueued on `stream`
+ *   before the call (so device indices written there are read safely) and ends
+ *   before anything enqueued on `stream` after the call returns.  Index arrays,
+ *   pools and staging buffers must stay valid until `stream` has passed the
+ *   call.  Calls that share a staging buffer must be ordered by the caller.
+ *
+ * Errors:
+ *   Every function returns a hicache_status and never aborts or throws across
+ *   the ABI.  hicache_last_error() returns a per-thread message for the last
+ *   non-OK status.  Argument and index validation complete before any copy is
+ *   enqueued, so a rejected call moves no byte.  A load call that fails still
+ *   records every layer-done event it was given on `stream`.
+ */
+#ifndef HICACHE_H
+#define HICACHE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define HICACHE_ABI_VERSION 1
+
+typedef enum hicache_status {
+  HICACHE_OK = 0,
+  HICACHE_EINVAL = 1,   /* bad argument: null pointer, bad shape, layer range, pool mismatch,
+                           pool memory the GPU cannot address, page-granular pairs that are not
+                           whole aligned pages */
+  HICACHE_ERANGE = 2,   /* an index is negative or beyond its pool */
+  HICACHE_EDUP = 3,     /* two pairs name the same destination row */
+  HICACHE_EALIGN = 4,   /* row bytes not a multiple of 4, or a base pointer not 4-byte aligned */
+  HICACHE_ECUDA = 5,    /* a CUDA runtime call failed; hicache_last_error() names it */
+  HICACHE_ENOSTAGE = 6  /* the staged path was requested without usable staging buffers */
+} hicache_status;
+
+typedef enum hicache_path {
+  HICACHE_PATH_AUTO = 0,      /* the library chooses per call from row size, run length, direction */
+  HICACHE_PATH_ZERO_COPY = 1, /* SMs read and write the mapped pinned host pool directly */
+  HICACHE_PATH_STAGED = 2     /* gather/scatter through HBM staging + copy-engine DMA */
+} hicache_path;
+
+typedef enum hicache_index_location {
+  /* Both index arrays are in pinned (page-locked) host memory: the CPU validates
+   * them completely before enqueueing (range, duplicate destinations, whole
+   * pages) and the GPU reads them through their mapping. */
+  HICACHE_INDEX_HOST = 0,
+  /* Both index arrays are in device memory and may still be being written on
+   * `stream`.  The CPU does not read them: kernels skip pairs that are out of
+   * range (or, for a page-granular pool, not page-aligned) and OR an error bit
+   * into opts->device_error when given.  Distinct destinations are the caller's
+   * responsibility in this mode. */
+  HICACHE_INDEX_DEVICE = 1
+} hicache_index_location;
+
+/* Bits kernels OR into hicache_opts.device_error. */
+#define HICACHE_DEVERR_RANGE 1u     /* a pair was out of range and skipped */
+#define HICACHE_DEVERR_PAGE_ALIGN 2u /* a page-granular pair was not page-aligned and skipped */
+
+typedef struct hicache_pool {
+  int32_t num_layers;     /* L: layers of this pool */
+  int32_t num_tensors;    /* T: 2 = MHA K and V, 1 = MLA latent or DSA indexer */
+  int32_t head_num;       /* KV heads per token row (1 for MLA latent and indexer) */
+  int32_t head_dim;       /* elements per head (576 for MLA latent, 132 for the indexer) */
+  int32_t dtype_size;     /* bytes per element (2 for bf16, 1 for uint8/fp8) */
+  int32_t page_size;      /* P: tokens per page, the same for device and host */
+  int32_t page_granular;  /* 1: pairs must cover whole page-aligned pages (DSA indexer) */
+  int32_t reserved;       /* must be 0 */
+  int64_t device_slots;   /* token rows per device layer buffer */
+  int64_t host_pages;     /* pages of the host pool */
+  void* const* device_layers; /* host array of T * L device pointers, [t * L + l] */
+  void* const* host_tensors;  /* host array of T pinned host pointers (page-first) */
+} hicache_pool;
+
+typedef struct hicache_opts {
+  int32_t path;            /* hicache_path */
+  int32_t index_location;  /* hicache_index_location */
+  int32_t max_ctas;        /* 0 = library default; else caps the CTAs of each copy kernel so that
+                              a concurrent consumer keeps the remaining SMs */
+  int32_t reserved;        /* must be 0 */
+  void* staging[2];        /* staged path: two device buffers used alternately */
+  size_t staging_bytes;    /* bytes of each staging buffer */
+  cudaStream_t copy_stream;/* staged path: stream for the DMA copies (0 = library-internal) */
+  uint32_t* device_error;  /* optional device-accessible word; kernels OR HICACHE_DEVERR_* bits */
+} hicache_opts;
+
+/*
+ * All-layer backup (device -> host) of the pairs device_indices[i] ->
+ * host_indices[i], i < n, for every layer and tensor of every pool.
+ * Passage: sglang PR #28434 summary, key source excerpts
+ * (backup_from_device_all_layer; CPU simulation of the staged lf->pf copy).
+ *   pools, num_pools : 1..4 pools that share the pair list, the layer count and
+ *                      the page size (e.g. MLA latent + DSA indexer-K).
+ *   device_indices, host_indices : n token indices each, int32 or int64
+ *                      (index_bits 32 or 64), located as opts->index_location.
+ *   opts             : NULL for defaults (AUTO path, host-located indices).
+ *   stream           : stream the work is ordered on.
+ * Host destinations must be distinct (HICACHE_EDUP); sources may repeat.
+ * Host bytes not named by a pair are never written.
+ */
+hicache_status hicache_backup_all_layers(const hicache_pool* pools, int32_t num_pools,
+                                         const void* device_indices, const void* host_indices,
+                                         int32_t index_bits, int64_t n,
+                                         const hicache_opts* opts, cudaStream_t stream);
+
+/*
+ * Load-back (host -> device) of one layer: host_indices[i] -> device_indices[i]
+ * for layer `layer` of every tensor of every pool.  If layer_done is not NULL
+ * it is recorded on `stream` after the copies, also when the call fails.
+ * Passage: sglang PR #38472, Motivation (per-layer load_to_device_per_layer)
+ * and Modifications (every layer event completes on failure).
+ * Device destinations must be distinct (HICACHE_EDUP); sources may repeat.
+ */
+hicache_status hicache_load_layer(const hicache_pool* pools, int32_t num_pools, int32_t layer,
+                                  const void* host_indices, const void* device_indices,
+                                  int32_t index_bits, int64_t n, const hicache_opts* opts,
+                                  cudaStream_t stream, cudaEvent_t layer_done);
+
+/*
+ * Load-back burst: layers layer_begin .. layer_end-1 in increasing order, each
+ * followed by cudaEventRecord(layer_done[l - layer_begin], stream), so event l
+ * means every pool's layer l has landed.  The indices are validated once for
+ * the whole burst.  layer_done holds layer_end - layer_begin events (entries
+ * may be NULL).  On any failure every non-NULL event is still recorded.
+ * Passage: sglang PR #38472, Motivation (one burst of per-layer loads gated by
+ * LayerDoneCounter.wait_until) and Modifications (failure completes every
+ * layer event).
+ */
+hicache_status hicache_load_burst(const hicache_pool* pools, int32_t num_pools,
+                                  int32_t layer_begin, int32_t layer_end,
+                                  const void* host_indices, const void* device_indices,
+                                  int32_t index_bits, int64_t n, const hicache_opts* opts,
+                                  cudaStream_t stream, cudaEvent_t* layer_done);
+
+/* One maximal run of pairs: device slots d0.., host slots h0.., len pairs. */
+typedef struct hicache_run {
+  int64_t d0;
+  int64_t h0;
+  int64_t len;
+} hicache_run;
+
+/*
+ * Run planner (host only; no CUDA call).  Splits n pairs in host memory into
+ * maximal runs in which the device and the host slot both increase by one and
+ * the host slot does not cross a page boundary.  Writes up to runs_cap runs and
+ * stores the total count in *num_runs (runs_out may be NULL to count only) and,
+ * if full_pages is not NULL, the number of runs that are one whole page-aligned
+ * host page.  Replaces the per-chunk CPU copy descriptors that the per-layer
+ * load builds (sglang PR #38472, Motivation).
+ */
+hicache_status hicache_plan_runs(const void* device_indices, const void* host_indices,
+                                 int32_t index_bits, int64_t n, int32_t page_size,
+                                 hicache_run* runs_out, int64_t runs_cap, int64_t* num_runs,
+                                 int64_t* full_pages);
+
+/*
+ * Synthetic consumer (not a transfer): adds, over the pairs' device slots
+ * device_indices[i], i < n, of layer `layer` of tensor `tensor` of `pool`, every
+ * little-endian 32-bit word of each row into *out_sum (device memory, a uint64
+ * the caller zeroes), modulo 2^64.  Used to show that a kernel gated by a
+ * layer-done event sees that layer fully loaded.  R must be a multiple of 4;
+ * indices must be device memory.  No counterpart in the pages: it stands in for
+ * the attention layer that waits on the layer event.
+ */
+hicache_status hicache_layer_checksum(const hicache_pool* pool, int32_t tensor, int32_t layer,
+                                      const void* device_indices, int32_t index_bits, int64_t n,
+                                      uint64_t* out_sum, cudaStream_t stream);
+
+/* Number of kernels this library has launched in this process (all threads and
+ * devices).  Lets a caller count the GPU work a region of its program issued. */
+int64_t hicache_kernel_launches(void);
+
+/* Message for the last non-OK status returned on the calling thread. */
+const char* hicache_last_error(void);
+
+/* HICACHE_ABI_VERSION of the loaded library. */
+int32_t hicache_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* HICACHE_H */

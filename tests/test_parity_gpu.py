@@ -1,0 +1,340 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle, bit for bit.
+
+Every test compares whole pools (every byte, touched or not) unless stated.
+Sizes span many warp tasks and end in ragged tails; edge cases cover empty
+lists, partial pages, 4-byte rows, non-power-of-two page sizes, page-granular
+pools, more segments than one launch holds, grid-stride loops, device-located
+indices with bad entries, failures that must still record every layer event,
+and the full Llama-3-8B-shaped workload in the launch configuration the
+benchmark uses.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import hierarchical_kv_cache_gb300 as hk  # noqa: E402
+from hierarchical_kv_cache_gb300 import workloads as W  # noqa: E402
+from tests import gpu_helpers as G  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from hierarchical_kv_cache_gb300.build import build
+
+    build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+
+
+def _opts(path, where, **kw):
+    loc = hk.HICACHE_INDEX_DEVICE if where == "device" else hk.HICACHE_INDEX_HOST
+    return hk.Opts(path=path, index_location=loc, **kw)
+
+
+def _staging(nbytes):
+    return [torch.empty(nbytes, dtype=torch.uint8, device="cuda") for _ in range(2)]
+
+
+# ---------------------------------------------------------------- tiny MHA pool
+
+@pytest.mark.parametrize("where", ["device", "host"])
+@pytest.mark.parametrize("dtype", [torch.int32, torch.int64])
+@pytest.mark.parametrize("path", ["zero_copy", "staged"])
+def test_tiny_mha_backup_then_load(where, dtype, path):
+    wl = W.tiny_mha()
+    s = wl.pools[0]
+    if path == "staged" and where == "device":
+        pytest.skip("the staged path plans DMA spans on the CPU: host-located indices only")
+    pool = G.make_pool(s, seed=wl.seed)
+    d, h, dp, hp = W.page_pairs(wl.seed, wl.move_pages, s.device_slots // s.page_size,
+                                s.host_pages, s.page_size)
+    dev0, host0 = G.device_images(pool), G.host_images(pool)
+    dt, ht = G.index_tensors(d, h, where, dtype)
+    if path == "staged":
+        # room for 5 host pages of all layers: 64 pages take 13 chunks, both buffers alternate
+        per_page = s.num_tensors * s.num_layers * s.page_size * s.row_bytes
+        opts = _opts(hk.HICACHE_PATH_STAGED, where, staging=_staging(5 * per_page))
+    else:
+        opts = _opts(hk.HICACHE_PATH_ZERO_COPY, where)
+    hk.hicache_backup_all_layers(pool, dt, ht, opts=opts)
+    torch.cuda.synchronize()
+    G.oracle_backup(pool, dev0, host0, d, h)
+    G.assert_host_equal(pool, host0, "backup")
+
+    # load back into fresh random device pages (distinct from the source pages)
+    d2, _, _, _ = W.page_pairs(wl.seed + 100, wl.move_pages, s.device_slots // s.page_size,
+                               s.host_pages, s.page_size, exclude_device_pages=dp)
+    d2t, _ = G.index_tensors(d2, h, where, dtype)
+    dev1 = G.device_images(pool)
+    events = [torch.cuda.Event() for _ in range(s.num_layers)]
+    hk.hicache_load_burst(pool, 0, s.num_layers, ht, d2t, opts=opts, layer_done=events)
+    torch.cuda.synchronize()
+    assert all(e.query() for e in events)
+    G.oracle_load(pool, dev1, host0, range(s.num_layers), h, d2)
+    G.assert_device_equal(pool, dev1, "load burst")
+    # round trip: the fresh slots hold the original rows
+    for t in range(s.num_tensors):
+        for l in range(s.num_layers):
+            a = dev0[t][l].reshape(-1, s.row_bytes)[d]
+            b = pool.device_layers[t][l].cpu().numpy().reshape(-1, s.row_bytes)[d2]
+            assert np.array_equal(a, b)
+
+
+# ------------------------------------------------------ ragged shapes and tails
+
+CASES = [
+    # (L, T, head_num, head_dim, dtype_size, P, slots, pages, n, fragmented)
+    (3, 2, 1, 6, 2, 3, 300, 70, 157, True),       # 12-byte rows (4-byte path), P=3
+    (2, 1, 1, 8, 2, 1, 5000, 4000, 3001, True),    # 16-byte rows, token-random, P=1
+    (2, 2, 4, 8, 2, 16, 8192, 600, 4099, True),    # 64-byte rows, ragged final page
+    (4, 1, 1, 576, 2, 64, 4096, 80, 64 * 37 + 13, True),  # MLA rows, partial last page
+    (2, 2, 8, 128, 2, 64, 8192, 128, 64 * 40, False),     # one contiguous run of 40 pages
+    (5, 1, 1, 1024, 2, 256, 4096, 12, 256 * 7 + 100, True),  # P=256
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"R{c[2]*c[3]*c[4]}_P{c[5]}_n{c[8]}" for c in CASES])
+@pytest.mark.parametrize("where", ["device", "host"])
+def test_ragged_backup_and_load(case, where):
+    L, T, hn, hd, ds, P, slots, pages, n, frag = case
+    s = G.shape(L=L, T=T, head_num=hn, head_dim=hd, dtype_size=ds, P=P, slots=slots, pages=pages)
+    pool = G.make_pool(s, seed=n)
+    d, h = W.token_pairs(n + 1, n, slots, pages * P, P, fragmented=frag)
+    g = np.random.default_rng(n)
+    d = d.copy()
+    d[g.integers(0, n, size=n // 7)] = d[0]  # backup sources may repeat
+    dev0, host0 = G.device_images(pool), G.host_images(pool)
+    dt, ht = G.index_tensors(d, h, where)
+    hk.hicache_backup_all_layers(pool, dt, ht, opts=_opts(hk.HICACHE_PATH_ZERO_COPY, where))
+    torch.cuda.synchronize()
+    G.oracle_backup(pool, dev0, host0, d, h)
+    G.assert_host_equal(pool, host0, "backup")
+    # load: distinct device destinations, host sources may repeat
+    d2 = g.permutation(slots)[:n].astype(np.int64)
+    h2 = h.copy()
+    h2[g.integers(0, n, size=n // 5)] = h[-1]
+    dev1 = G.device_images(pool)
+    d2t, h2t = G.index_tensors(d2, h2, where)
+    for l in (L - 1, 0):
+        hk.hicache_load_layer(pool, l, h2t, d2t, opts=_opts(hk.HICACHE_PATH_ZERO_COPY, where))
+    torch.cuda.synchronize()
+    G.oracle_load(pool, dev1, host0, (L - 1, 0), h2, d2)
+    G.assert_device_equal(pool, dev1, "load")
+
+
+def test_grid_stride_and_many_segments():
+    """Three CTAs loop over many tasks; 600 segments need two launches of the all-layer kernel."""
+    s = G.shape(L=300, T=2, head_num=1, head_dim=8, dtype_size=2, P=4, slots=256, pages=40)
+    pool = G.make_pool(s, seed=5)
+    d, h = W.token_pairs(6, 150, 256, 160, 4, fragmented=True)
+    dev0, host0 = G.device_images(pool), G.host_images(pool)
+    dt, ht = G.index_tensors(d, h, "device")
+    hk.hicache_backup_all_layers(pool, dt, ht, opts=_opts(hk.HICACHE_PATH_ZERO_COPY, "device",
+                                                          max_ctas=3))
+    torch.cuda.synchronize()
+    G.oracle_backup(pool, dev0, host0, d, h)
+    G.assert_host_equal(pool, host0, "backup 600 segments")
+    dev1 = G.device_images(pool)
+    hk.hicache_load_burst(pool, 10, 290, ht, dt, opts=_opts(hk.HICACHE_PATH_ZERO_COPY, "device",
+                                                            max_ctas=1))
+    torch.cuda.synchronize()
+    G.oracle_load(pool, dev1, host0, range(10, 290), h, d)
+    G.assert_device_equal(pool, dev1, "burst")
+
+
+# ------------------------------------------------------- MLA + DSA indexer pools
+
+def _mla_dsa_shapes(L=5, P=64, pages=24, slots=64 * 40):
+    lat = G.shape("mla", L=L, T=1, head_num=1, head_dim=576, dtype_size=2, P=P, slots=slots,
+                  pages=pages)
+    idx = G.shape("dsa", L=L, T=1, head_num=1, head_dim=132, dtype_size=1, P=P, slots=slots,
+                  pages=pages, page_granular=True, value_kind="uint8_uniform")
+    return lat, idx
+
+
+@pytest.mark.parametrize("path", ["zero_copy", "staged"])
+def test_two_pools_mla_and_indexer(path):
+    lat_s, idx_s = _mla_dsa_shapes()
+    pools = [G.make_pool(lat_s, 7), G.make_pool(idx_s, 8)]
+    P = lat_s.page_size
+    d, h, dp, hp = W.page_pairs(9, 9, lat_s.device_slots // P, lat_s.host_pages, P)
+    imgs = [(G.device_images(p), G.host_images(p)) for p in pools]
+    dt, ht = G.index_tensors(d, h, "host")
+    if path == "staged":
+        per_page = sum(p.num_layers * P * p.row_bytes for p in pools)
+        opts = _opts(hk.HICACHE_PATH_STAGED, "host", staging=_staging(2 * per_page + 4096))
+    else:
+        opts = _opts(hk.HICACHE_PATH_ZERO_COPY, "host")
+    hk.hicache_backup_all_layers(pools, dt, ht, opts=opts)
+    torch.cuda.synchronize()
+    for p, (dev0, host0) in zip(pools, imgs):
+        G.oracle_backup(p, dev0, host0, d, h)
+        G.assert_host_equal(p, host0, "two-pool backup")
+    d2, _, _, _ = W.page_pairs(10, 9, lat_s.device_slots // P, lat_s.host_pages, P,
+                               exclude_device_pages=dp)
+    d2t, _ = G.index_tensors(d2, h, "host")
+    dev1s = [G.device_images(p) for p in pools]
+    events = [torch.cuda.Event() for _ in range(lat_s.num_layers)]
+    hk.hicache_load_burst(pools, 0, lat_s.num_layers, ht, d2t, opts=opts, layer_done=events)
+    torch.cuda.synchronize()
+    for p, dev1, (_, host0) in zip(pools, dev1s, imgs):
+        G.oracle_load(p, dev1, host0, range(p.num_layers), h, d2)
+        G.assert_device_equal(p, dev1, "two-pool burst")
+
+
+def test_indexer_rejects_partial_pages_on_device():
+    """Device-located indices: a page-granular pool skips unaligned pages and flags them."""
+    _, idx_s = _mla_dsa_shapes(L=2)
+    pool = G.make_pool(idx_s, 11)
+    P = idx_s.page_size
+    d = np.concatenate([np.arange(P) + 3 * P, np.arange(P) + 5 * P + 1]).astype(np.int64)
+    h = np.concatenate([np.arange(P) + 2 * P, np.arange(P) + 7 * P]).astype(np.int64)
+    dev0, host0 = G.device_images(pool), G.host_images(pool)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dt, ht = G.index_tensors(d, h, "device")
+    hk.hicache_backup_all_layers(pool, dt, ht, opts=_opts(hk.HICACHE_PATH_ZERO_COPY, "device",
+                                                          device_error=err))
+    torch.cuda.synchronize()
+    assert int(err.item()) == hk.HICACHE_DEVERR_PAGE_ALIGN
+    G.oracle_backup(pool, dev0, host0, d[:P], h[:P])  # only the aligned page moves
+    G.assert_host_equal(pool, host0, "indexer aligned page only")
+
+
+# ----------------------------------------------------------------- error paths
+
+def test_device_indices_out_of_range_are_skipped_and_flagged():
+    s = G.shape(L=2, T=2, head_num=2, head_dim=64, dtype_size=2, P=16, slots=1024, pages=64)
+    pool = G.make_pool(s, 12)
+    d, h = W.token_pairs(13, 500, 1024, 1024, 16, fragmented=True)
+    d = d.copy()
+    d[17] = 5000  # out of range
+    h = h.copy()
+    h[300] = -4
+    dev0, host0 = G.device_images(pool), G.host_images(pool)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dt, ht = G.index_tensors(d, h, "device")
+    hk.hicache_backup_all_layers(pool, dt, ht, opts=_opts(hk.HICACHE_PATH_ZERO_COPY, "device",
+                                                          device_error=err))
+    torch.cuda.synchronize()
+    assert int(err.item()) == hk.HICACHE_DEVERR_RANGE
+    keep = np.ones(500, dtype=bool)
+    keep[[17, 300]] = False
+    G.oracle_backup(pool, dev0, host0, d[keep], h[keep])
+    G.assert_host_equal(pool, host0, "skipped bad pairs")
+
+
+def test_failed_burst_still_records_every_event():
+    s = G.shape(L=6, T=2, head_num=2, head_dim=64, dtype_size=2, P=16, slots=1024, pages=64)
+    pool = G.make_pool(s, 14)
+    d, h = W.token_pairs(15, 64, 1024, 1024, 16, fragmented=True)
+    dev0 = G.device_images(pool)
+    h = h.copy()
+    h[5] = 10 ** 6  # out of range: validation fails on the host
+    dt, ht = G.index_tensors(d, h, "host")
+    events = [torch.cuda.Event() for _ in range(4)]
+    for e in events:
+        e.record()
+    torch.cuda.synchronize()
+    torch.cuda._sleep(200_000_000)  # keep the stream busy so a fresh record is observable
+    with pytest.raises(hk.HiCacheError) as ei:
+        hk.hicache_load_burst(pool, 1, 5, ht, dt, layer_done=events)
+    assert ei.value.status == hk.HICACHE_ERANGE
+    assert not any(e.query() for e in events), "events were not re-recorded behind the sleep"
+    torch.cuda.synchronize()
+    assert all(e.query() for e in events)
+    G.assert_device_equal(pool, dev0, "rejected burst moved bytes")
+
+
+def test_duplicate_destination_rejected_and_nothing_moves():
+    s = G.shape(L=2, T=1, head_num=1, head_dim=64, dtype_size=2, P=4, slots=256, pages=16)
+    pool = G.make_pool(s, 16)
+    host0 = G.host_images(pool)
+    dt, ht = G.index_tensors([1, 2, 3], [5, 6, 5], "host")
+    with pytest.raises(hk.HiCacheError) as ei:
+        hk.hicache_backup_all_layers(pool, dt, ht)
+    assert ei.value.status == hk.HICACHE_EDUP
+    torch.cuda.synchronize()
+    G.assert_host_equal(pool, host0, "rejected backup moved bytes")
+
+
+def test_staged_needs_staging_and_whole_pages():
+    s = G.shape(L=2, T=2, head_num=2, head_dim=64, dtype_size=2, P=16, slots=1024, pages=64)
+    pool = G.make_pool(s, 17)
+    d, h = W.token_pairs(18, 40, 1024, 1024, 16, fragmented=True)  # 40 tokens: partial page
+    dt, ht = G.index_tensors(d, h, "host")
+    with pytest.raises(hk.HiCacheError) as ei:
+        hk.hicache_backup_all_layers(pool, dt, ht, opts=_opts(hk.HICACHE_PATH_STAGED, "host"))
+    assert ei.value.status == hk.HICACHE_ENOSTAGE
+    with pytest.raises(hk.HiCacheError) as ei:
+        hk.hicache_backup_all_layers(pool, dt, ht, opts=_opts(hk.HICACHE_PATH_STAGED, "host",
+                                                              staging=_staging(1 << 20)))
+    assert ei.value.status == hk.HICACHE_EINVAL
+
+
+def test_empty_lists_record_events_and_move_nothing():
+    s = G.shape(L=3, T=2, head_num=2, head_dim=64, dtype_size=2, P=16, slots=1024, pages=64)
+    pool = G.make_pool(s, 19)
+    dev0, host0 = G.device_images(pool), G.host_images(pool)
+    dt, ht = G.index_tensors(np.zeros(0, np.int64), np.zeros(0, np.int64), "device")
+    events = [torch.cuda.Event() for _ in range(3)]
+    hk.hicache_backup_all_layers(pool, dt, ht)
+    hk.hicache_load_burst(pool, 0, 3, ht, dt, layer_done=events)
+    torch.cuda.synchronize()
+    assert all(e.query() for e in events)
+    G.assert_device_equal(pool, dev0, "empty")
+    G.assert_host_equal(pool, host0, "empty")
+
+
+# ----------------------------------------------------- events gate a consumer
+
+def test_layer_events_gate_consumer_checksum():
+    """A consumer on another stream waits on event l only, and must see layer l fully loaded."""
+    s = G.shape("mla", L=12, T=1, head_num=1, head_dim=576, dtype_size=2, P=64, slots=65536,
+                pages=512)
+    pool = G.make_pool(s, 20)
+    d, h, _, _ = W.page_pairs(21, 256, s.device_slots // 64, s.host_pages, 64)
+    host0 = G.host_images(pool)
+    dt, ht = G.index_tensors(d, h, "device")
+    events = [torch.cuda.Event() for _ in range(s.num_layers)]
+    sums = torch.zeros(s.num_layers, dtype=torch.int64, device="cuda")
+    consumer = torch.cuda.Stream()
+    load_stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(load_stream):
+        hk.hicache_load_burst(pool, 0, s.num_layers, ht, dt, layer_done=events,
+                              stream=load_stream)
+    for l in range(s.num_layers):
+        consumer.wait_event(events[l])
+        hk.hicache_layer_checksum(pool, 0, l, dt, sums[l:l + 1], stream=consumer)
+    torch.cuda.synchronize()
+    R = s.row_bytes
+    for l in range(s.num_layers):
+        blk = host0[0].reshape(s.host_pages, s.num_layers, 64, R)[h // 64, l, h % 64]
+        want = int(blk.reshape(-1).view("<u4").astype(np.uint64).sum(dtype=np.uint64))
+        assert (int(sums[l].item()) & (2 ** 64 - 1)) == want, f"layer {l} checksum"
+
+
+# ------------------------------------------- full Llama-3-8B-shaped workload
+
+def test_llama3_8b_full_size_backup_and_burst():
+    """Full-size pools, the launch configuration the benchmark times; every byte compared."""
+    wl = W.llama3_8b_mha()
+    s = wl.pools[0]
+    P = s.page_size
+    pool = G.make_pool(s, wl.seed)
+    d, h, dp, hp = W.page_pairs(wl.seed, wl.move_pages, s.device_slots // P, s.host_pages, P)
+    d2, _, _, _ = W.page_pairs(wl.seed + 1, wl.move_pages, s.device_slots // P, s.host_pages, P,
+                               exclude_device_pages=dp)
+    dev0, host0 = G.device_images(pool), G.host_images(pool)
+    dt, ht = G.index_tensors(d, h, "device")
+    d2t, _ = G.index_tensors(d2, h, "device")
+    events = [torch.cuda.Event() for _ in range(s.num_layers)]
+    hk.hicache_backup_all_layers(pool, dt, ht)
+    hk.hicache_load_burst(pool, 0, s.num_layers, ht, d2t, layer_done=events)
+    torch.cuda.synchronize()
+    G.oracle_backup(pool, dev0, host0, d, h)
+    G.assert_host_equal(pool, host0, "full-size backup")
+    G.oracle_load(pool, dev0, host0, range(s.num_layers), h, d2)
+    G.assert_device_equal(pool, dev0, "full-size burst")
