@@ -29,7 +29,6 @@ import statistics
 import subprocess
 import sys
 import tempfile
-import threading
 import time
 
 import numpy as np
@@ -45,7 +44,7 @@ GB = 1e9
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama3_8b_mha")
@@ -56,6 +55,15 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--out", default=None, help="also append the JSON line to this file")
+    ap.add_argument("--pages", type=int, default=0,
+                    help="override the pages moved per op (smaller profiling cases)")
+    ap.add_argument("--device-slots", type=int, default=0, help="override device slots per pool")
+    ap.add_argument("--host-pages", type=int, default=0, help="override host pages per pool")
+    ap.add_argument("--sweep", action="store_true",
+                    help="run the row-size / page-size / length / fragmentation sweep instead")
+    ap.add_argument("--sweep-rows", default="16,64,256,1152,2048")
+    ap.add_argument("--sweep-pages", default="1,16,64,256")
+    ap.add_argument("--sweep-tokens", default="1024,4096,16384,65536,262144")
     return ap.parse_args()
 
 
@@ -176,11 +184,46 @@ def measure_link_peak(nbytes=1 << 30, reps=5):
     return out
 
 
+def hbm_peak():
+    """Measured HBM copy bandwidth of the GB300s, else the recipe's fallback."""
+    try:
+        with open(os.path.join(REPO, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"])
+    except (OSError, KeyError, ValueError):
+        return 6800.0
+
+
+def traffic_per_launch(which, algorithmic_bytes):
+    """DRAM bytes (read + write) per launch from the committed ncu record, scaled to this
+    launch's algorithmic bytes; None when the kernel source changed since the capture."""
+    import hashlib
+    try:
+        with open(os.path.join(REPO, "profiles", "row_copy_kernel_traffic.json")) as f:
+            rec = json.load(f)
+        src = open(os.path.join(REPO, "hierarchical_kv_cache_gb300", "csrc", "zero_copy.cu"),
+                   "rb").read()
+    except (OSError, ValueError):
+        return None
+    if hashlib.sha256(src).hexdigest()[:16] != rec.get("source_sha256_16"):
+        return None
+    c = rec["launches"][which]
+    per_byte = (c["dram_read_bytes"] + c["dram_write_bytes"]) / c["algorithmic_bytes"]
+    return int(per_byte * algorithmic_bytes)
+
+
 # ---------------------------------------------------------------- workload
 
-def build_workload(name, seed_offset=0):
+def build_workload(name, seed_offset=0, args=None):
+    import dataclasses
+
     from hierarchical_kv_cache_gb300 import workloads as W
     wl = W.WORKLOADS[name]()
+    if args is not None and (args.pages or args.device_slots or args.host_pages):
+        pools = tuple(dataclasses.replace(
+            s, device_slots=args.device_slots or s.device_slots,
+            host_pages=args.host_pages or s.host_pages) for s in wl.pools)
+        wl = dataclasses.replace(wl, pools=pools, move_pages=args.pages or wl.move_pages,
+                                 name=wl.name + " [resized for profiling]")
     s0 = wl.pools[0]
     P = s0.page_size
     dev_pages = min(s.device_slots for s in wl.pools) // P
@@ -206,7 +249,7 @@ def run_ours(args, rank, world):
     from hierarchical_kv_cache_gb300.build import build
 
     build()
-    wl, d, h, d2 = build_workload(args.workload)
+    wl, d, h, d2 = build_workload(args.workload, args=args)
     L = wl.pools[0].num_layers
     n = d.size
     t_alloc = time.time()
@@ -303,6 +346,17 @@ def run_ours(args, rank, world):
     total_ms = max_over_ranks(total_ms, world)
     value = world * K * step_bytes / (total_ms * 1e-3) / GB
 
+    # host enqueue cost of one burst, measured on an idle stream (while the timed
+    # loop runs ahead, a full launch queue would block the host and inflate it)
+    enq_idle = []
+    for _ in range(5):
+        stream.synchronize()
+        t0 = time.perf_counter()
+        hk.hicache_load_burst(pools, 0, L, idx_l[0], idx_l[1], opts=opts, stream=stream,
+                              layer_done=warm_events)
+        enq_idle.append(time.perf_counter() - t0)
+        stream.synchronize()
+
     mb, ml = statistics.mean(t_backup), statistics.mean(t_load)
     backup_gbs = bytes_backup / (mb * 1e-3) / GB
     load_gbs = bytes_load / (ml * 1e-3) / GB
@@ -328,7 +382,7 @@ def run_ours(args, rank, world):
             "step": "all-layer D2H backup + H2D per-layer load-back burst with layer events",
             "step_payload_bytes": int(step_bytes), "path": args.path,
             "index_location": "device (HBM)" if args.path != "staged" else "host (pinned)",
-            "l2": "inputs larger than L2 (8 GiB pools each side), no flush",
+            "l2": "inputs larger than L2 (pools of GiBs on each side), no flush",
             "parallelism": f"replicas x{world}",
             "host_alloc_s": round(t_alloc, 1),
         },
@@ -343,15 +397,32 @@ def run_ours(args, rank, world):
             "first_layer_event_us": round(first_us, 1),
             "first_event_bound_us": round(bound_us, 1),
             "first_event_within_bound": first_us <= bound_us,
-            "enqueue_us_per_layer": round(statistics.median(enq) * 1e6 / L, 2),
+            "enqueue_us_per_layer": round(statistics.median(enq_idle) * 1e6 / L, 2),
+            "enqueue_us_per_layer_queue_full": round(statistics.median(enq) * 1e6 / L, 2),
             "link_peak_gbs": {k: round(v, 2) for k, v in link.items()},
         },
         "roofline": {
+            "bound": "host_link", "achieved": round(backup_gbs, 2), "peak": round(link["d2h"], 2),
+            "unit": "GB/s", "frac": round(backup_gbs / link["d2h"], 4),
+            "traffic": traffic_per_launch("backup_all_layers", bytes_backup),
+            "kernel": "row_copy_kernel<int64,16,512>: one all-layer backup launch "
+                      f"({bytes_backup} algorithmic bytes = n x L x T x R)",
+            "peak_source": "pinned cudaMemcpyAsync D2H measured in this run (of measured); "
+                           "HBM is not the bound: the launch reads its payload once from HBM",
+            "hbm_frac_of_measured": round(backup_gbs / hbm_peak(), 4),
+        },
+        "roofline_load": {
+            "bound": "host_link", "achieved": round(layer_gbs, 2) if layer_gbs else None,
+            "peak": round(link["h2d"], 2), "unit": "GB/s",
+            "frac": round(layer_gbs / link["h2d"], 4) if layer_gbs else None,
+            "traffic": traffic_per_launch("load_one_layer", bytes_layer),
+            "kernel": "row_copy_kernel<int64,16,8>: one per-layer load launch "
+                      f"({bytes_layer} algorithmic bytes = n x T x R), median of the burst",
+        },
+        "roofline_step": {
             "bound": "host_link", "achieved": round(achieved, 2), "peak": round(peak_mix, 2),
-            "unit": "GB/s", "frac": round(achieved / peak_mix, 4), "traffic": None,
-            "kernel": "row_copy_kernel (all launches of one step)",
-            "peak_source": "pinned cudaMemcpyAsync D2H/H2D measured in this run, weighted by "
-                           "the step's bytes per direction",
+            "unit": "GB/s", "frac": round(achieved / peak_mix, 4),
+            "peak_source": "in-run D2H/H2D peaks weighted by the step's bytes per direction",
         },
         "gpu_launches": int(launches),
         "clocks": clk,
@@ -445,7 +516,7 @@ def cpu_baseline(wl, d, h, d2, seconds):
 def run_reference(args, rank, world):
     if rank != 0:
         return None
-    wl, d, h, d2 = build_workload(args.workload)
+    wl, d, h, d2 = build_workload(args.workload, args=args)
     dev_imgs, host_imgs = oracle_images(wl)
     pages = max(1, min(wl.move_pages, 16))
     for _ in range(args.warmup):
@@ -467,8 +538,111 @@ def run_reference(args, rank, world):
     }
 
 
+# ---------------------------------------------------------------- sweep
+
+def _time_op(fn, stream, min_ms=20.0, max_reps=200):
+    """Mean device ms of fn() over enough repetitions to fill min_ms."""
+    import torch
+    fn()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    fn()
+    e1.record(stream)
+    e1.synchronize()
+    one = max(e0.elapsed_time(e1), 1e-3)
+    reps = int(max(3, min(max_reps, min_ms / one)))
+    e0.record(stream)
+    for _ in range(reps):
+        fn()
+    e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def run_sweep(args):
+    """Config 5: bytes per row x page size x tokens x contiguity x direction x path."""
+    import torch
+    import hierarchical_kv_cache_gb300 as hk
+    from hierarchical_kv_cache_gb300 import workloads as W
+    from hierarchical_kv_cache_gb300._binding import Pool
+    from hierarchical_kv_cache_gb300.build import build
+
+    build()
+    torch.cuda.set_device(0)
+    rows = [int(x) for x in args.sweep_rows.split(",")]
+    psizes = [int(x) for x in args.sweep_pages.split(",")]
+    tokens = [int(x) for x in args.sweep_tokens.split(",")]
+    L = 4
+    link = measure_link_peak()
+    stream = torch.cuda.Stream()
+    staging = [torch.empty(args.staging_mib << 20, dtype=torch.uint8, device="cuda")
+               for _ in range(2)]
+    events = [torch.cuda.Event() for _ in range(L)]
+    out = []
+    nmax = max(tokens)
+    for R in rows:
+        slots = 2 * nmax
+        dev = [[torch.empty(slots * R, dtype=torch.uint8, device="cuda") for _ in range(L)]]
+        host = [torch.empty(slots * L * R, dtype=torch.uint8, pin_memory=True)]
+        for buf in dev[0]:
+            buf.random_(0, 256)
+        for P in psizes:
+            pool = Pool(device_layers=dev, host_tensors=host, num_layers=L, head_num=1,
+                        head_dim=R // 2, dtype_size=2, page_size=P, device_slots=slots,
+                        host_pages=slots // P)
+            for n in tokens:
+                for frag in (False, True):
+                    d, h = W.token_pairs(1000 + n + P, n, slots, slots, P, fragmented=frag)
+                    runs, full = hk.hicache_plan_runs(d, h, P)
+                    dt = torch.as_tensor(d).cuda()
+                    htd = torch.as_tensor(h).cuda()
+                    dth = torch.as_tensor(d).pin_memory()
+                    hth = torch.as_tensor(h).pin_memory()
+                    nbytes = n * L * R
+                    for path in ("zero_copy", "staged"):
+                        whole = (n % P == 0 and full == n // P) or P == 1
+                        spans = len(runs) if frag else 1
+                        if path == "staged" and (not whole or spans > 8192):
+                            continue
+                        if path == "zero_copy":
+                            o = hk.Opts(path=hk.HICACHE_PATH_ZERO_COPY,
+                                        index_location=hk.HICACHE_INDEX_DEVICE)
+                            ib, il = (dt, htd), (htd, dt)
+                        else:
+                            o = hk.Opts(path=hk.HICACHE_PATH_STAGED,
+                                        index_location=hk.HICACHE_INDEX_HOST, staging=staging)
+                            ib, il = (dth, hth), (hth, dth)
+                        t_b = _time_op(lambda: hk.hicache_backup_all_layers(
+                            pool, ib[0], ib[1], opts=o, stream=stream), stream)
+                        t_l = _time_op(lambda: hk.hicache_load_burst(
+                            pool, 0, L, il[0], il[1], opts=o, stream=stream,
+                            layer_done=events), stream)
+                        for direction, t, peak in (("d2h_backup", t_b, link["d2h"]),
+                                                   ("h2d_burst", t_l, link["h2d"])):
+                            gbs = nbytes / (t * 1e-3) / GB
+                            rec = {"row_bytes": R, "page_size": P, "tokens": n,
+                                   "fragmented": frag, "runs": int(len(runs)),
+                                   "direction": direction, "path": path, "layers": L,
+                                   "ms": round(t, 4), "gbs": round(gbs, 2),
+                                   "frac_of_link": round(gbs / peak, 4)}
+                            out.append(rec)
+                            print(json.dumps(rec), flush=True)
+        del dev, host
+        torch.cuda.synchronize()
+    if args.out:
+        with open(args.out, "w") as f:
+            for rec in out:
+                f.write(json.dumps(rec) + "\n")
+    print(json.dumps({"sweep_points": len(out), "link_peak_gbs": link}), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.sweep:
+        run_sweep(args)
+        return
     if args.impl == "reference":
         rank = int(os.environ.get("RANK", "0"))
         world = int(os.environ.get("WORLD_SIZE", "1"))
