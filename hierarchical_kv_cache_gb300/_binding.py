@@ -69,6 +69,8 @@ def lib():
         L.hicache_plan_runs.argtypes = [vp, vp, i32, i64, i32, ctypes.POINTER(c_run), i64,
                                         ctypes.POINTER(i64), ctypes.POINTER(i64)]
         L.hicache_layer_checksum.argtypes = [P, i32, i32, vp, i32, i64, vp, vp]
+        L.hicache_backup_all_layers_static_staging.argtypes = [P, i32, vp, vp, i32, i64, O, vp]
+        L.hicache_backup_all_layers_static_staging.restype = ctypes.c_int
         for f in ("hicache_backup_all_layers", "hicache_load_layer", "hicache_load_burst",
                   "hicache_plan_runs", "hicache_layer_checksum"):
             getattr(L, f).restype = ctypes.c_int
@@ -219,6 +221,24 @@ def hicache_backup_all_layers(pools, device_indices, host_indices, *, opts: Opti
     _check(lib().hicache_backup_all_layers(arr, npools, device_indices.data_ptr(),
                                            host_indices.data_ptr(), bits, n, ctypes.byref(o),
                                            _stream_arg(stream)))
+
+
+def hicache_backup_all_layers_static_staging(pools, device_indices, host_indices, *,
+                                             opts: Optional[Opts] = None, stream=None) -> None:
+    """All-layer backup through the staged path using the library's own static staging.
+
+    For callers that cannot allocate device memory when they transfer (for
+    example an engine that gave all free HBM to its KV pool at start-up): no
+    staging buffer is passed and nothing is allocated.  Indices must be pinned
+    host tensors covering whole host pages; one host page of all layers must fit
+    in 16 MiB.  Calls that overlap on the GPU share the static array and race.
+    """
+    arr, npools, _ = _pools_arg(pools)
+    bits, n = _indices(device_indices, host_indices)
+    o = _opts_arg(opts, device_indices, host_indices)
+    _check(lib().hicache_backup_all_layers_static_staging(
+        arr, npools, device_indices.data_ptr(), host_indices.data_ptr(), bits, n,
+        ctypes.byref(o), _stream_arg(stream)))
 
 
 def hicache_load_layer(pools, layer: int, host_indices, device_indices, *,

@@ -8,6 +8,7 @@
 // loader thread" (Modifications: a failed load completes every layer event).
 #include <cuda_runtime.h>
 
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -224,6 +225,81 @@ extern "C" hicache_status hicache_load_burst(const hicache_pool* pools, int32_t 
     return st;
   }
   return load_layers(pr, layer_begin, layer_end, stream, layer_done);
+}
+
+// ---------------------------------------------------------------------------
+// Backup with library-owned staging memory, for callers that cannot allocate.
+//
+// The staging lives in a file-scope device array.  Host code must not use the
+// array's name as a device address (in host code it names a host-side
+// stand-in); the device address is resolved once per device with
+// cudaGetSymbolAddress and handed to the staged backup as its two buffers.
+
+static __device__ __align__(256) unsigned char g_static_staging[HICACHE_STATIC_STAGING_BYTES];
+
+namespace hk {
+namespace {
+
+std::mutex g_static_mu;
+void* g_static_addr[64] = {};
+
+// Device address of g_static_staging on the current device (resolved once).
+hicache_status static_staging_address(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(HICACHE_EINVAL, "device ordinal above 63");
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_staging);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static staging array)");
+    if (!p) return fail(HICACHE_ECUDA, "cudaGetSymbolAddress returned NULL for the staging array");
+    g_static_addr[dev] = p;
+  }
+  *out = g_static_addr[dev];
+  return HICACHE_OK;
+}
+
+}  // namespace
+}  // namespace hk
+
+extern "C" hicache_status hicache_backup_all_layers_static_staging(
+    const hicache_pool* pools, int32_t num_pools, const void* device_indices,
+    const void* host_indices, int32_t index_bits, int64_t n, const hicache_opts* opts,
+    cudaStream_t stream) {
+  clear_error();
+  hicache_opts o = opts ? *opts : default_opts();
+  // Pure host checks first, so that a rejected call touches no CUDA state.
+  std::vector<PoolInfo> checked;
+  hicache_status st = check_pools(pools, num_pools, &checked);
+  if (st != HICACHE_OK) return st;
+  constexpr int64_t kHalf = int64_t(HICACHE_STATIC_STAGING_BYTES) / 2;
+  int64_t page_all_layers = 0;
+  for (const PoolInfo& pi : checked)
+    page_all_layers += int64_t(pi.T) * pi.L * pi.P * pi.token_bytes;
+  if (page_all_layers > kHalf)
+    return fail(HICACHE_ENOSTAGE, "one host page of all layers of all pools is " +
+                                      std::to_string(page_all_layers) +
+                                      " bytes, above the " + std::to_string(kHalf) +
+                                      "-byte half of the static staging array");
+  if (n == 0) {
+    Prepared pr;
+    return prepare(pools, num_pools, device_indices, host_indices, index_bits, n, &o,
+                   /*dest_is_device=*/false, false, 0, 0, &pr);
+  }
+  void* base = nullptr;
+  st = static_staging_address(&base);
+  if (st != HICACHE_OK) return st;
+  o.path = HICACHE_PATH_STAGED;
+  o.staging[0] = base;
+  o.staging[1] = static_cast<unsigned char*>(base) + kHalf;
+  o.staging_bytes = size_t(kHalf);
+  Prepared pr;
+  st = prepare(pools, num_pools, device_indices, host_indices, index_bits, n, &o,
+               /*dest_is_device=*/false, false, 0, 0, &pr);
+  if (st != HICACHE_OK) return st;
+  return staged_backup(pr.pools, pr.o, pr.idx, stream);
 }
 
 extern "C" hicache_status hicache_plan_runs(const void* device_indices, const void* host_indices,

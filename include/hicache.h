@@ -175,6 +175,43 @@ hicache_status hicache_load_burst(const hicache_pool* pools, int32_t num_pools,
                                   int32_t index_bits, int64_t n, const hicache_opts* opts,
                                   cudaStream_t stream, cudaEvent_t* layer_done);
 
+/* Bytes of the library's own device staging array used by
+ * hicache_backup_all_layers_static_staging: two halves of 16 MiB. */
+#define HICACHE_STATIC_STAGING_BYTES (32u << 20)
+
+/*
+ * All-layer backup through the staged path without any memory from the caller
+ * or the CUDA allocator.  Same pairs, pools, result and errors as
+ * hicache_backup_all_layers with HICACHE_PATH_STAGED, but the two staging
+ * buffers are the halves of one device array of HICACHE_STATIC_STAGING_BYTES
+ * that the library defines statically (every GPU that loads the library holds
+ * it until the process exits).  The pages have no counterpart for this entry
+ * point: it exists for callers that cannot allocate device memory at transfer
+ * time, such as a serving engine that reserved all free HBM for its KV pool at
+ * start-up, or a thin C caller with no device allocator of its own.
+ *   - The call allocates nothing: no cudaMalloc, no cudaFree, no allocating
+ *     library routine.  opts->staging and opts->staging_bytes are ignored.
+ *   - Host-located indices covering whole host pages are required, as for the
+ *     staged path (HICACHE_EINVAL otherwise).
+ *   - One host page of all layers of all pools must fit in one 16 MiB half;
+ *     larger pages are rejected with HICACHE_ENOSTAGE and a message giving both
+ *     sizes.  Any number of pages is handled, 16 MiB at a time.
+ *   - The first call on a device (with that device current) resolves the
+ *     array's device address, and the first call on a thread and device creates
+ *     the internal copy stream and events; make that first call before any
+ *     stream capture.
+ *   - Every call uses the same array.  Nothing in it needs to start at zero:
+ *     each call writes every staging byte it copies out.  Calls that overlap on
+ *     the GPU (for example on two streams without ordering) race on the array.
+ */
+hicache_status hicache_backup_all_layers_static_staging(const hicache_pool* pools,
+                                                        int32_t num_pools,
+                                                        const void* device_indices,
+                                                        const void* host_indices,
+                                                        int32_t index_bits, int64_t n,
+                                                        const hicache_opts* opts,
+                                                        cudaStream_t stream);
+
 /* One maximal run of pairs: device slots d0.., host slots h0.., len pairs. */
 typedef struct hicache_run {
   int64_t d0;
