@@ -52,6 +52,10 @@ def _bind(lib):
     lib.oracle_load_layer.restype = ctypes.c_int
     lib.oracle_load_burst.argtypes = [i64, i64, i64, i64, i64, i64, i64, vp, vp, vp, vp, i64]
     lib.oracle_load_burst.restype = ctypes.c_int
+    lib.oracle_pf_backup_all_layers.argtypes = [i64, i64, i64, i64, vp, vp, vp, vp, i64]
+    lib.oracle_pf_backup_all_layers.restype = ctypes.c_int
+    lib.oracle_pf_load_layer.argtypes = [i64, i64, i64, i64, i64, vp, vp, vp, vp, i64]
+    lib.oracle_pf_load_layer.restype = ctypes.c_int
     return lib
 
 
@@ -132,3 +136,36 @@ def load_burst(device_layers, host, layer_begin: int, layer_end: int, host_idx, 
                                layer_begin, layer_end, ctypes.cast(arr, ctypes.c_void_p),
                                _ptr(host), _ptr(h), _ptr(d), d.size)
     _check(rc, "oracle_load_burst")
+
+
+def pf_backup_all_layers(device_layers, host, device_idx, host_idx, *, row_bytes: int,
+                         lib=None) -> None:
+    """Oracle all-layer backup into a page_first ([token][layer][row]) host tensor."""
+    lib = lib or load()
+    L = len(device_layers)
+    assert host.dtype == np.uint8 and host.flags.c_contiguous
+    d = _idx(device_idx)
+    h = _idx(host_idx)
+    assert d.shape == h.shape
+    device_slots = device_layers[0].size // row_bytes
+    host_tokens = host.size // (L * row_bytes)
+    arr = _layers_array(device_layers)
+    rc = lib.oracle_pf_backup_all_layers(L, row_bytes, device_slots, host_tokens,
+                                         ctypes.cast(arr, ctypes.c_void_p), _ptr(host), _ptr(d),
+                                         _ptr(h), d.size)
+    _check(rc, "oracle_pf_backup_all_layers")
+
+
+def pf_load_layer(device_layer, host, layer: int, host_idx, device_idx, *, num_layers: int,
+                  row_bytes: int, lib=None) -> None:
+    """Oracle load-back of one layer from a page_first host tensor."""
+    lib = lib or load()
+    assert device_layer.dtype == np.uint8 and device_layer.flags.c_contiguous
+    d = _idx(device_idx)
+    h = _idx(host_idx)
+    assert d.shape == h.shape
+    device_slots = device_layer.size // row_bytes
+    host_tokens = host.size // (num_layers * row_bytes)
+    rc = lib.oracle_pf_load_layer(num_layers, row_bytes, device_slots, host_tokens, layer,
+                                  _ptr(device_layer), _ptr(host), _ptr(h), _ptr(d), d.size)
+    _check(rc, "oracle_pf_load_layer")

@@ -90,3 +90,46 @@ int oracle_load_burst(int64_t num_layers, int64_t page_size, int64_t row_bytes,
   }
   return ORACLE_OK;
 }
+
+/* ---- page_first host layout: [host token][layer][row] ---------------------- */
+
+/* Byte offset of host token h, layer l, in the token-major host tensor: the
+ * staging shape (token, layer, element) of the staged write-back. */
+static int64_t pf_host_row_offset(int64_t h, int64_t l, int64_t num_layers, int64_t row_bytes) {
+  return (h * num_layers + l) * row_bytes;
+}
+
+int oracle_pf_backup_all_layers(int64_t num_layers, int64_t row_bytes, int64_t device_slots,
+                                int64_t host_tokens, const uint8_t* const* device_layers,
+                                uint8_t* host, const int64_t* device_idx, const int64_t* host_idx,
+                                int64_t n) {
+  if (!shape_ok(num_layers, 1, row_bytes, device_slots, host_tokens, n)) return ORACLE_BAD_ARG;
+  if (n > 0 && (!device_layers || !host || !device_idx || !host_idx)) return ORACLE_BAD_ARG;
+  if (!pairs_in_range(device_idx, host_idx, n, device_slots, host_tokens)) return ORACLE_OUT_OF_RANGE;
+  /* dst[dst_indices, layer] = src[src_indices], one layer after the other */
+  for (int64_t l = 0; l < num_layers; ++l) {
+    const uint8_t* src_layer = device_layers[l];
+    for (int64_t i = 0; i < n; ++i) {
+      const uint8_t* src = src_layer + device_row_offset(device_idx[i], row_bytes);
+      uint8_t* dst = host + pf_host_row_offset(host_idx[i], l, num_layers, row_bytes);
+      memcpy(dst, src, (size_t)row_bytes);
+    }
+  }
+  return ORACLE_OK;
+}
+
+int oracle_pf_load_layer(int64_t num_layers, int64_t row_bytes, int64_t device_slots,
+                         int64_t host_tokens, int64_t layer, uint8_t* device_layer,
+                         const uint8_t* host, const int64_t* host_idx, const int64_t* device_idx,
+                         int64_t n) {
+  if (!shape_ok(num_layers, 1, row_bytes, device_slots, host_tokens, n)) return ORACLE_BAD_ARG;
+  if (layer < 0 || layer >= num_layers) return ORACLE_BAD_ARG;
+  if (n > 0 && (!device_layer || !host || !device_idx || !host_idx)) return ORACLE_BAD_ARG;
+  if (!pairs_in_range(device_idx, host_idx, n, device_slots, host_tokens)) return ORACLE_OUT_OF_RANGE;
+  for (int64_t i = 0; i < n; ++i) {
+    const uint8_t* src = host + pf_host_row_offset(host_idx[i], layer, num_layers, row_bytes);
+    uint8_t* dst = device_layer + device_row_offset(device_idx[i], row_bytes);
+    memcpy(dst, src, (size_t)row_bytes);
+  }
+  return ORACLE_OK;
+}

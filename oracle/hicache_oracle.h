@@ -83,6 +83,26 @@ int oracle_load_burst(int64_t num_layers, int64_t page_size, int64_t row_bytes,
                       uint8_t* const* device_layers, const uint8_t* host,
                       const int64_t* host_idx, const int64_t* device_idx, int64_t n);
 
+/*
+ * The page_first host layout: token-major, [host token][layer][row].  It is the
+ * shape of the staging buffer in "[HiCache] Support hybrid-pool staged
+ * write-back JIT kernel" (sglang PR #28434 summary), key source excerpts
+ * (staging_token_capacity x layer_num x element_dim), on which the CPU
+ * simulation writes dst[dst_indices, layer] = src[src_indices].  Host token h
+ * of layer l starts at byte (h * num_layers + l) * row_bytes; pages play no
+ * part in the addressing (a page is page_size consecutive tokens).
+ *   host_tokens : tokens of the host tensor (host_pages * page_size).
+ */
+int oracle_pf_backup_all_layers(int64_t num_layers, int64_t row_bytes, int64_t device_slots,
+                                int64_t host_tokens, const uint8_t* const* device_layers,
+                                uint8_t* host, const int64_t* device_idx, const int64_t* host_idx,
+                                int64_t n);
+
+int oracle_pf_load_layer(int64_t num_layers, int64_t row_bytes, int64_t device_slots,
+                         int64_t host_tokens, int64_t layer, uint8_t* device_layer,
+                         const uint8_t* host, const int64_t* host_idx, const int64_t* device_idx,
+                         int64_t n);
+
 #ifdef __cplusplus
 }
 #endif

@@ -17,7 +17,10 @@ with:
 - structural facts of page-first storage read off tagged rows: one host page is
   one contiguous block holding exactly its own tokens for every layer, layer
   blocks in increasing layer order, tokens in increasing in-page order;
-- a burst equals its layers loaded one by one, in order.
+- a burst equals its layers loaded one by one, in order;
+- for the page_first (token-major) layout: a hand-worked golden image, the
+  pages' CPU simulation itself on a [token][layer][row] array, the round trip
+  with untouched-byte counts, and token-major structure read off tagged rows.
 
 ``run_all_pins`` collects failures instead of stopping at the first, so the
 planted-mutation controls can require that every mutant fails some pin.
@@ -233,6 +236,83 @@ def pin_burst_is_layer_sequence(lib):
         assert np.array_equal(a[l], b[l]), f"burst layer {l}"
 
 
+# ---- page_first host layout: [host token][layer][row] ---------------------
+
+def pin_pf_golden(lib):
+    fx = gf.parse("pf_backup_L3_R2.txt")
+    L, P, R = fx["num_layers"], fx["page_size"], fx["row_bytes"]
+    dev = gf.device_image(fx)
+    host = np.full(fx["host_pages"] * P * L * R, int(fx["host_fill"], 16), dtype=np.uint8)
+    oracle.pf_backup_all_layers(dev, host, fx["device_idx"], fx["host_idx"], row_bytes=R, lib=lib)
+    assert np.array_equal(host, gf.rows_image(fx["expected_host"])), "page_first golden differs"
+
+
+def pin_pf_numpy_shape(lib):
+    """The pages' CPU simulation itself: dst[dst_indices, layer] = src[src_indices]."""
+    g = np.random.default_rng(21)
+    for (L, P, R, S, H, n) in SHAPES:
+        tokens = H * P
+        dev, host = _pool(g, L, P, R, S, H)
+        d = g.integers(0, S, size=n).astype(np.int64)
+        h = _distinct(g, tokens, n)
+        got = host.copy()
+        oracle.pf_backup_all_layers(dev, got, d, h, row_bytes=R, lib=lib)
+        want = host.copy().reshape(tokens, L, R)
+        for l in range(L):
+            want[h, l] = dev[l].reshape(S, R)[d]
+        assert np.array_equal(got, want.reshape(-1)), f"pf backup vs numpy {(L, P, R)}"
+        dd = _distinct(g, S, n)
+        hh = g.integers(0, tokens, size=n).astype(np.int64)
+        host3 = host.reshape(tokens, L, R)
+        for l in range(L):
+            got_l = dev[l].copy()
+            oracle.pf_load_layer(got_l, host, l, hh, dd, num_layers=L, row_bytes=R, lib=lib)
+            want_l = dev[l].copy().reshape(S, R)
+            want_l[dd] = host3[hh, l]
+            assert np.array_equal(got_l, want_l.reshape(-1)), f"pf load vs numpy {(L, P, R, l)}"
+
+
+def pin_pf_round_trip_and_untouched(lib):
+    g = np.random.default_rng(22)
+    for (L, P, R, S, H, n) in SHAPES:
+        tokens = H * P
+        dev = [(g.integers(0, 128, size=S * R, dtype=np.uint8) * 2 + 1).astype(np.uint8)
+               for _ in range(L)]
+        host = np.zeros(tokens * L * R, dtype=np.uint8)
+        d = _distinct(g, S, n)
+        h = _distinct(g, tokens, n)
+        oracle.pf_backup_all_layers(dev, host, d, h, row_bytes=R, lib=lib)
+        assert int(np.count_nonzero(host)) == n * L * R, "pf backup changed bytes"
+        fresh = [np.zeros(S * R, dtype=np.uint8) for _ in range(L)]
+        d2 = _distinct(g, S, n)
+        for l in range(L):
+            oracle.pf_load_layer(fresh[l], host, l, h, d2, num_layers=L, row_bytes=R, lib=lib)
+            assert int(np.count_nonzero(fresh[l])) == n * R, "pf load changed bytes"
+            assert np.array_equal(fresh[l].reshape(S, R)[d2], dev[l].reshape(S, R)[d])
+
+
+def pin_pf_structure(lib):
+    """Token-major storage read off tagged rows: each token holds its L layers in order."""
+    g = np.random.default_rng(23)
+    L, R, S, tokens, n = 4, 8, 64, 40, 25
+    dev = _tag_rows(L, S, R)
+    host = np.zeros(tokens * L * R, dtype=np.uint8)
+    h = _distinct(g, tokens, n)
+    d = _distinct(g, S, n)
+    oracle.pf_backup_all_layers(dev, host, d, h, row_bytes=R, lib=lib)
+    rows = host.reshape(tokens, L, R)
+    slot_of = dict(zip(h.tolist(), d.tolist()))
+    for tok in range(tokens):
+        blk = rows[tok]
+        if tok not in slot_of:
+            assert not blk.any(), f"untouched token {tok} written"
+            continue
+        lay = blk[:, 0:2].copy().view("<u2").reshape(-1).tolist()
+        slot = blk[:, 2:6].copy().view("<u4").reshape(-1).tolist()
+        assert lay == list(range(L)), f"layers of token {tok} out of order"
+        assert slot == [slot_of[tok]] * L, f"token {tok} holds the wrong slot"
+
+
 PINS = [
     pin_golden_backup,
     pin_golden_load,
@@ -243,6 +323,10 @@ PINS = [
     pin_boundary_page_counts,
     pin_layout_structure,
     pin_burst_is_layer_sequence,
+    pin_pf_golden,
+    pin_pf_numpy_shape,
+    pin_pf_round_trip_and_untouched,
+    pin_pf_structure,
 ]
 
 

@@ -37,6 +37,12 @@ MUTANTS = {
                          "for (int64_t l = layer_begin + 1; l < layer_end; ++l) {"),
     "short_row": ("memcpy(dst, src, (size_t)row_bytes);\n    }\n  }",
                   "memcpy(dst, src, (size_t)row_bytes - 1);\n    }\n  }"),
+    "pf_layer_major": ("return (h * num_layers + l) * row_bytes;",
+                       "return (l * num_layers + h) * row_bytes;"),
+    "pf_dropped_layer_term": ("return (h * num_layers + l) * row_bytes;",
+                              "return (h * num_layers) * row_bytes;"),
+    "pf_load_reads_layer0": ("pf_host_row_offset(host_idx[i], layer, num_layers, row_bytes)",
+                             "pf_host_row_offset(host_idx[i], 0, num_layers, row_bytes)"),
     "device_slot_of_host": ("const uint8_t* src = src_layer + device_row_offset(device_idx[i], row_bytes);",
                             "const uint8_t* src = src_layer + device_row_offset(host_idx[i] % device_slots, row_bytes);"),
 }
