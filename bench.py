@@ -51,6 +51,8 @@ def parse_args():
     ap.add_argument("--path", choices=["auto", "zero_copy", "staged"], default="auto")
     ap.add_argument("--staging-mib", type=int, default=256)
     ap.add_argument("--max-ctas", type=int, default=0)
+    ap.add_argument("--burst", choices=["per_layer", "single_launch"], default="single_launch",
+                    help="load burst as one kernel launch per layer, or one launch for all layers")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -271,6 +273,8 @@ def run_ours(args, rank, world):
                    for _ in range(2)]
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     stream = torch.cuda.Stream()
+    words = (torch.zeros(4 * L, dtype=torch.int32, device="cuda")
+             if args.burst == "single_launch" else None)
 
     # device-resident indices for the device-timed value
     dt = torch.as_tensor(d).cuda()
@@ -283,11 +287,11 @@ def run_ours(args, rank, world):
     if args.path == "staged":
         idx_b, idx_l = (dt_h, ht_h), (ht_h, d2t_h)
         opts = hk.Opts(path=path, index_location=hk.HICACHE_INDEX_HOST, staging=staging,
-                       max_ctas=args.max_ctas, device_error=err)
+                       max_ctas=args.max_ctas, device_error=err, burst_words=words)
     else:
         idx_b, idx_l = (dt, ht_dev), (ht_dev, d2t)
         opts = hk.Opts(path=path, index_location=hk.HICACHE_INDEX_DEVICE, staging=staging,
-                       max_ctas=args.max_ctas, device_error=err)
+                       max_ctas=args.max_ctas, device_error=err, burst_words=words)
 
     link = measure_link_peak()
     bytes_backup, bytes_layer = payload_bytes(wl, n)
@@ -369,7 +373,8 @@ def run_ours(args, rank, world):
 
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(hk, pools, wl, dt_h, ht_h, d2t_h, L, staging, path, args, step_bytes, n)
+        e2e = run_e2e(hk, pools, wl, dt_h, ht_h, d2t_h, L, staging, path, args, step_bytes, n,
+                      words)
 
     res = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
@@ -380,7 +385,7 @@ def run_ours(args, rank, world):
             "workload": wl.name, "description": wl.description,
             "pages_per_op": wl.move_pages, "tokens_per_op": int(n), "layers": L,
             "step": "all-layer D2H backup + H2D per-layer load-back burst with layer events",
-            "step_payload_bytes": int(step_bytes), "path": args.path,
+            "step_payload_bytes": int(step_bytes), "path": args.path, "burst": args.burst,
             "index_location": "device (HBM)" if args.path != "staged" else "host (pinned)",
             "l2": "inputs larger than L2 (pools of GiBs on each side), no flush",
             "parallelism": f"replicas x{world}",
@@ -416,8 +421,11 @@ def run_ours(args, rank, world):
             "peak": round(link["h2d"], 2), "unit": "GB/s",
             "frac": round(layer_gbs / link["h2d"], 4) if layer_gbs else None,
             "traffic": traffic_per_launch("load_one_layer", bytes_layer),
-            "kernel": "row_copy_kernel<int64,16,8>: one per-layer load launch "
-                      f"({bytes_layer} algorithmic bytes = n x T x R), median of the burst",
+            "kernel": ("row_copy_kernel<int64,16,8>: one per-layer load launch"
+                       if args.burst == "per_layer" else
+                       "row_copy_kernel<int64,16,512,signalling>: one layer of the "
+                       "single-launch burst (event-to-event)")
+                      + f" ({bytes_layer} algorithmic bytes = n x T x R), median of the burst",
         },
         "roofline_step": {
             "bound": "host_link", "achieved": round(achieved, 2), "peak": round(peak_mix, 2),
@@ -434,13 +442,13 @@ def run_ours(args, rank, world):
     return res
 
 
-def run_e2e(hk, pools, wl, dt_h, ht_h, d2t_h, L, staging, path, args, step_bytes, n):
+def run_e2e(hk, pools, wl, dt_h, ht_h, d2t_h, L, staging, path, args, step_bytes, n, words):
     """Public-API step with pinned host indices (host validation included) and a D2H status read."""
     import torch
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     err_h = torch.zeros(1, dtype=torch.int32).pin_memory()
     opts = hk.Opts(path=path, index_location=hk.HICACHE_INDEX_HOST, staging=staging,
-                   max_ctas=args.max_ctas, device_error=err)
+                   max_ctas=args.max_ctas, device_error=err, burst_words=words)
     events = [torch.cuda.Event() for _ in range(L)]
     stream = torch.cuda.Stream()
 
@@ -580,6 +588,7 @@ def run_sweep(args):
     staging = [torch.empty(args.staging_mib << 20, dtype=torch.uint8, device="cuda")
                for _ in range(2)]
     events = [torch.cuda.Event() for _ in range(L)]
+    words = torch.zeros(4 * L, dtype=torch.int32, device="cuda")
     out = []
     nmax = max(tokens)
     for R in rows:
@@ -608,7 +617,9 @@ def run_sweep(args):
                             continue
                         if path == "zero_copy":
                             o = hk.Opts(path=hk.HICACHE_PATH_ZERO_COPY,
-                                        index_location=hk.HICACHE_INDEX_DEVICE)
+                                        index_location=hk.HICACHE_INDEX_DEVICE,
+                                        burst_words=words if args.burst == "single_launch"
+                                        else None)
                             ib, il = (dt, htd), (htd, dt)
                         else:
                             o = hk.Opts(path=hk.HICACHE_PATH_STAGED,
@@ -625,6 +636,7 @@ def run_sweep(args):
                             rec = {"row_bytes": R, "page_size": P, "tokens": n,
                                    "fragmented": frag, "runs": int(len(runs)),
                                    "direction": direction, "path": path, "layers": L,
+                                   "burst": args.burst if path == "zero_copy" else "per_layer",
                                    "ms": round(t, 4), "gbs": round(gbs, 2),
                                    "frac_of_link": round(gbs / peak, 4)}
                             out.append(rec)

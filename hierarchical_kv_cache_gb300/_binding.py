@@ -41,7 +41,8 @@ class c_opts(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int32), ("index_location", ctypes.c_int32),
                 ("max_ctas", ctypes.c_int32), ("reserved", ctypes.c_int32),
                 ("staging", ctypes.c_void_p * 2), ("staging_bytes", ctypes.c_size_t),
-                ("copy_stream", ctypes.c_void_p), ("device_error", ctypes.c_void_p)]
+                ("copy_stream", ctypes.c_void_p), ("device_error", ctypes.c_void_p),
+                ("burst_words", ctypes.c_void_p), ("burst_words_len", ctypes.c_int64)]
 
 
 class c_run(ctypes.Structure):
@@ -149,6 +150,7 @@ class Opts:
     staging: Optional[Sequence] = None  # two device tensors
     copy_stream: Optional[object] = None  # torch.cuda.Stream
     device_error: Optional[object] = None  # int32/uint32 tensor of one element
+    burst_words: Optional[object] = None  # int32 CUDA tensor, >= 4 words per burst layer
 
 
 def _pools_arg(pools):
@@ -182,6 +184,9 @@ def _opts_arg(opts: Optional[Opts], a, b):
         c.copy_stream = o.copy_stream.cuda_stream
     if o.device_error is not None:
         c.device_error = o.device_error.data_ptr()
+    if o.burst_words is not None:
+        c.burst_words = o.burst_words.data_ptr()
+        c.burst_words_len = o.burst_words.numel() * o.burst_words.element_size() // 4
     return c
 
 

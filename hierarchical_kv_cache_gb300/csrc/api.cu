@@ -12,6 +12,7 @@
 #include <string>
 #include <vector>
 
+#include "burst.h"
 #include "hicache_internal.h"
 #include "staged.h"
 
@@ -117,15 +118,29 @@ hicache_status prepare(const hicache_pool* pools, int32_t num_pools, const void*
   return HICACHE_OK;
 }
 
+// Host-only checks of opts->burst_words for a burst of `count` layers.
+hicache_status check_burst_words(const hicache_opts& o, int32_t count) {
+  if (!o.burst_words) return HICACHE_OK;
+  if (o.burst_words_len < kBurstWordsPerLayer * int64_t(count))
+    return fail(HICACHE_EINVAL, "opts.burst_words holds " + std::to_string(o.burst_words_len) +
+                                    " words; the burst needs " +
+                                    std::to_string(kBurstWordsPerLayer) + " per layer (" +
+                                    std::to_string(kBurstWordsPerLayer * int64_t(count)) + ")");
+  if (reinterpret_cast<uintptr_t>(o.burst_words) % 4 != 0)
+    return fail(HICACHE_EALIGN, "opts.burst_words is not 4-byte aligned");
+  return HICACHE_OK;
+}
+
 SideSpec host_side(const std::vector<PoolInfo>& pools) {
   SideSpec s;
-  s.vec16 = vec16_ok(pools);
   s.layer_origin = 0;
   for (const PoolInfo& pi : pools) {
+    const int64_t layer_stride = int64_t(pi.P) * pi.token_bytes;
     s.base.push_back(pi.host);
-    s.layer_stride.push_back(int64_t(pi.P) * pi.token_bytes);
+    s.layer_stride.push_back(layer_stride);
     s.page_stride.push_back(int64_t(pi.L) * pi.P * pi.token_bytes);
     s.paged_tokens.push_back(pi.host_pages * pi.P);
+    s.vec16.push_back(vec16_ok(pi, pi.host, layer_stride));
   }
   return s;
 }
@@ -150,6 +165,8 @@ hicache_status load_layers(const Prepared& pr, int32_t layer_begin, int32_t laye
   if (path == HICACHE_PATH_STAGED)
     return staged_load(pr.pools, pr.o, pr.idx, layer_begin, layer_end, stream, evs);
   const SideSpec side = host_side(pr.pools);
+  if (pr.o.burst_words && signaled_burst_available())
+    return signaled_burst(pr.pools, side, pr.idx, pr.o, layer_begin, layer_end, stream, evs);
   const LaunchCfg cfg = launch_cfg(pr.o);
   for (int32_t l = layer_begin; l < layer_end; ++l) {
     hicache_status st = launch_rows(pr.pools, side, pr.idx.dev_gpu, pr.idx.host_gpu, pr.idx.bits,
@@ -220,6 +237,7 @@ extern "C" hicache_status hicache_load_burst(const hicache_pool* pools, int32_t 
   Prepared pr;
   hicache_status st = prepare(pools, num_pools, device_indices, host_indices, index_bits, n, opts,
                               /*dest_is_device=*/true, true, layer_begin, layer_end, &pr);
+  if (st == HICACHE_OK) st = check_burst_words(pr.o, count);
   if (st != HICACHE_OK || n == 0) {
     record_events(layer_done, count, stream);
     return st;

@@ -1,0 +1,168 @@
+// burst.cu -- the single-launch load-back burst with per-layer events.
+//
+// The per-layer load-back of "[HiCache] Run the host->device load-back enqueue
+// on a loader thread" signals a layer-done event after each layer so that the
+// attention layer waiting on it can start early.  Launching one kernel per
+// layer pays a launch gap plus a ramp-up and a drain per layer.  Here one
+// launch of the row-copy kernel covers every layer of the burst (tasks in
+// layer order); the warp that completes a layer sets that layer's word in
+// device memory.  A library stream, forked from the caller's stream before the
+// launch, waits on each word in turn with a stream memory wait (handled by the
+// GPU front end, not by a spinning kernel) and records the caller's event for
+// that layer.  The caller's stream joins the library stream before the call
+// returns, so the whole burst stays ordered on the caller's stream.
+//
+// No wait can outlive the launch: the waits are enqueued only after the launch
+// succeeded, and the last CTA to leave the launch sets every word of its layers.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "burst.h"
+
+namespace hk {
+
+namespace {
+
+using WaitValue32Fn = CUresult(CUDAAPI*)(CUstream, CUdeviceptr, cuuint32_t, unsigned int);
+
+hicache_status cuda_fail(cudaError_t e, const std::string& what) {
+  return fail(HICACHE_ECUDA, what + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")");
+}
+
+// Library stream and events of the burst, created once per thread and device.
+struct BurstRes {
+  bool init = false;
+  cudaStream_t sig = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+WaitValue32Fn wait_value32() {
+  static std::once_flag once;
+  static WaitValue32Fn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuStreamWaitValue32", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<WaitValue32Fn>(p);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+hicache_status get_res(BurstRes** out) {
+  static thread_local BurstRes res[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(HICACHE_EINVAL, "device ordinal above 63");
+  BurstRes& r = res[dev];
+  if (!r.init) {
+    e = cudaStreamCreateWithFlags(&r.sig, cudaStreamNonBlocking);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamCreate(burst signal stream)");
+    e = cudaEventCreateWithFlags(&r.fork, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&r.join, cudaEventDisableTiming);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventCreate(burst)");
+    r.init = true;
+  }
+  *out = &r;
+  return HICACHE_OK;
+}
+
+void record_from(cudaEvent_t* evs, int32_t from, int32_t count, cudaStream_t s) {
+  if (!evs) return;
+  for (int32_t i = from; i < count; ++i)
+    if (evs[i]) cudaEventRecord(evs[i], s);
+}
+
+}  // namespace
+
+bool signaled_burst_available() { return wait_value32() != nullptr; }
+
+hicache_status signaled_burst(const std::vector<PoolInfo>& pools, const SideSpec& side,
+                              const IndexSet& idx, const hicache_opts& o, int32_t layer_begin,
+                              int32_t layer_end, cudaStream_t stream, cudaEvent_t* evs) {
+  const int32_t count = layer_end - layer_begin;
+  // With no row to move no kernel runs, so nothing would ever set the words.
+  int64_t rows = 0;
+  for (const PoolInfo& pi : pools) rows += pi.page_granular ? idx.n / pi.P : idx.n;
+  if (rows == 0) {
+    record_from(evs, 0, count, stream);
+    return HICACHE_OK;
+  }
+  WaitValue32Fn wait = wait_value32();
+  BurstRes* r = nullptr;
+  hicache_status st = wait ? get_res(&r)
+                           : fail(HICACHE_ECUDA, "cuStreamWaitValue32 is not available from the driver");
+  if (st != HICACHE_OK) {
+    record_from(evs, 0, count, stream);
+    return st;
+  }
+  const LaunchCfg cfg{o.max_ctas, o.device_error};
+  // The first layer is latency-critical (nothing downstream can start before
+  // it), so it gets a launch of its own and its event on the caller's stream;
+  // the remaining layers share one signalling launch.
+  int32_t first = 0;  // burst-relative index of the first signalled layer
+  if (count >= 2) {
+    st = launch_rows(pools, side, idx.dev_gpu, idx.host_gpu, idx.bits, 0, idx.n, kPagedToDev,
+                     layer_begin, layer_begin + 1, cfg, stream);
+    cudaError_t e0 = cudaSuccess;
+    if (st == HICACHE_OK && evs && evs[0]) e0 = cudaEventRecord(evs[0], stream);
+    if (st == HICACHE_OK && e0 != cudaSuccess) st = cuda_fail(e0, "cudaEventRecord(layer_done)");
+    if (st != HICACHE_OK) {
+      record_from(evs, 0, count, stream);
+      return st;
+    }
+    first = 1;
+  }
+  const int32_t nsig = count - first;
+  uint32_t* words = o.burst_words;
+  BurstWords bw{words, words + nsig, words + 2 * int64_t(nsig), words + 3 * int64_t(nsig)};
+  cudaError_t e = cudaMemsetAsync(words, 0, size_t(kBurstWordsPerLayer) * nsig * sizeof(uint32_t),
+                                  stream);
+  if (e == cudaSuccess) e = cudaEventRecord(r->fork, stream);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(r->sig, r->fork, 0);
+  if (e != cudaSuccess) {
+    st = cuda_fail(e, "burst set-up");
+    record_from(evs, first, count, stream);
+    return st;
+  }
+  st = launch_rows(pools, side, idx.dev_gpu, idx.host_gpu, idx.bits, 0, idx.n, kPagedToDev,
+                   layer_begin + first, layer_end, cfg, stream, &bw);
+  if (st != HICACHE_OK) {
+    // nothing waits on the words yet: complete the events on the caller's stream
+    record_from(evs, first, count, stream);
+    return st;
+  }
+  int32_t i = first;
+  for (; i < count; ++i) {
+    const CUresult cr = wait(reinterpret_cast<CUstream>(r->sig),
+                             reinterpret_cast<CUdeviceptr>(bw.flag + (i - first)), 1u,
+                             CU_STREAM_WAIT_VALUE_GEQ);
+    if (cr != CUDA_SUCCESS) {
+      st = fail(HICACHE_ECUDA, "cuStreamWaitValue32 failed with CUresult " + std::to_string(int(cr)));
+      break;
+    }
+    if (evs && evs[i]) {
+      e = cudaEventRecord(evs[i], r->sig);
+      if (e != cudaSuccess) {
+        st = cuda_fail(e, "cudaEventRecord(layer_done)");
+        break;  // evs[i] is recorded on the caller's stream below
+      }
+    }
+  }
+  // layers whose wait could not be enqueued complete after the launch, on the caller's stream
+  record_from(evs, i, count, stream);
+  e = cudaEventRecord(r->join, r->sig);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, r->join, 0);
+  if (e != cudaSuccess && st == HICACHE_OK) st = cuda_fail(e, "burst join");
+  return st;
+}
+
+}  // namespace hk

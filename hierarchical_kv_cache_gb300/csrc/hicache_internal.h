@@ -19,7 +19,9 @@ namespace hk {
 constexpr int kMaxPools = 4;
 constexpr int kWarpsPerCta = 8;     // 256-thread CTAs
 constexpr int kThreadsPerCta = kWarpsPerCta * 32;
-constexpr int kUnroll = 4;          // 16-byte chunks in flight per lane per iteration
+constexpr int kUnroll = 4;          // chunks in flight per lane per iteration
+constexpr int kMaxRowsPerTask = 128; // rows of one warp task (shared-memory offset table)
+constexpr int64_t kTaskBytes = 2048; // target payload of one warp task
 constexpr int kMaxSegSmall = 8;     // per-layer launches: pools x tensors
 constexpr int kMaxSegLarge = 512;   // all-layer launches: pools x tensors x layers
 
@@ -39,11 +41,11 @@ struct PoolGeom {
   int32_t rows_per_page;     // P for token pools, 1 for page-granular pools
   int32_t idx_stride;        // pair index of row k is k * idx_stride (P for page pools)
   int32_t idx_div;           // token index -> row index divisor (P for page pools)
-  int32_t rows_per_task;     // 1..32 rows handled by one warp task
-  uint32_t cpr;              // chunks (VEC bytes) per row
+  int32_t rows_per_task;     // 1..kMaxRowsPerTask rows handled by one warp task
+  uint32_t cpr;              // chunks (vec bytes) per row
   uint32_t q32, r32;         // 32 == q32 * cpr + r32
   uint32_t qS, rS;           // 32 * kUnroll == qS * cpr + rS
-  uint32_t pad;
+  uint32_t vec;              // chunk bytes: 16, or 4 when a row or base is not 16-aligned
 };
 
 // One (pool, tensor, layer) stream.
@@ -54,14 +56,34 @@ struct Segment {
   int32_t pad;
 };
 
+// Per-layer completion signalling of a single-launch burst.  Segments are
+// ordered layer-major, segs_per_layer per layer; layer k of the launch is
+// burst layer layer_base + k.  Words (device memory, zeroed before the launch):
+// done[burst layer] counts finished tasks, flag[burst layer] becomes 1 once
+// every task of that layer has landed; exits[launch first layer] counts CTAs
+// that left the launch and next[launch first layer] hands out its tasks.
+struct SignalSpec {
+  uint32_t* done = nullptr;
+  uint32_t* flag = nullptr;
+  uint32_t* exits = nullptr;
+  uint32_t* next = nullptr;
+  int64_t tasks_per_layer = 0;
+  int32_t segs_per_layer = 0;
+  int32_t layer_base = 0;   // burst-relative index of this launch's first layer
+  int32_t nlayers = 0;      // layers covered by this launch
+  int32_t pad = 0;
+};
+
 template <int MAXSEG>
 struct CopyParams {
+  static constexpr int kMaxSeg = MAXSEG;
   const void* dev_idx;      // device-slot indices (device-accessible)
   const void* paged_idx;    // paged-side token indices; NULL = pair index - pair_begin
   uint32_t* err;            // optional device-accessible error word
   int64_t pair_begin;       // first pair moved by this launch
   int32_t nseg;
   int32_t dir;              // Dir
+  SignalSpec sig;           // unused unless the kernel is the signalling instance
   PoolGeom pool[kMaxPools];
   int64_t seg_task_begin[MAXSEG + 1];
   Segment seg[MAXSEG];
@@ -116,7 +138,7 @@ struct LaunchCfg {
 // The page-first side of a launch: the pinned host pool, or an HBM staging
 // buffer laid out the same way.  Indexed [pool] and [pool][tensor].
 struct SideSpec {
-  bool vec16 = false;                     // 16-byte chunks usable on both sides
+  std::vector<bool> vec16;                // [pool] 16-byte chunks usable on both sides
   int32_t layer_origin = 0;               // layer whose block starts at base
   std::vector<std::vector<char*>> base;   // [pool][tensor] base address
   std::vector<int64_t> layer_stride;      // [pool] bytes between layer blocks of one page
@@ -125,15 +147,27 @@ struct SideSpec {
 };
 
 int64_t moved_row_bytes(const PoolInfo& pi);
-bool vec16_ok(const std::vector<PoolInfo>& pools);
+// 16-byte chunks are usable for pool `pi` against paged-side bases `paged_bases`
+// whose layer blocks are `layer_stride` bytes apart.
+bool vec16_ok(const PoolInfo& pi, const std::vector<char*>& paged_bases, int64_t layer_stride);
 void fill_geometry(const PoolInfo& pi, int64_t npairs, int vec, int64_t paged_page_stride,
                    int64_t paged_tokens, PoolGeom* g);
 // Moves pairs [pair_begin, pair_begin + npairs) for layers [layer_begin, layer_end)
-// of every pool and tensor between the device buffers and `side`.
+// of every pool and tensor between the device buffers and `side`.  With
+// `signal` (words of a single-launch burst: done, flag, exits, next, each
+// indexed by l - layer_begin), launches are cut at layer boundaries and every layer's flag
+// word is set once all of its rows have landed.
+struct BurstWords {
+  uint32_t* done = nullptr;
+  uint32_t* flag = nullptr;
+  uint32_t* exits = nullptr;
+  uint32_t* next = nullptr;
+};
 hicache_status launch_rows(const std::vector<PoolInfo>& pools, const SideSpec& side,
                            const void* dev_idx, const void* paged_idx, int32_t index_bits,
                            int64_t pair_begin, int64_t npairs, Dir dir, int32_t layer_begin,
-                           int32_t layer_end, const LaunchCfg& cfg, cudaStream_t stream);
+                           int32_t layer_end, const LaunchCfg& cfg, cudaStream_t stream,
+                           const BurstWords* signal = nullptr);
 hicache_status launch_checksum(const PoolInfo& pool, int32_t tensor, int32_t layer,
                                const void* dev_idx, int32_t index_bits, int64_t n,
                                uint64_t* out, cudaStream_t stream);

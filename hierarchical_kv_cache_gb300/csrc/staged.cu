@@ -56,14 +56,11 @@ hicache_status get_res(StagedRes** out) {
   return HICACHE_OK;
 }
 
-bool aligned16(const void* p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; }
-
 // Staging layout: one region per (pool, tensor), each `cap_pages` pages of
 // `page_bytes(pool)` bytes; region offsets are in (pool, tensor) order.
 struct StagingLayout {
   int64_t cap_pages = 0;
   std::vector<std::vector<int64_t>> region_off;  // [pool][tensor]
-  bool vec16 = false;
 };
 
 StagingLayout layout_for(const std::vector<PoolInfo>& pools, const hicache_opts& o,
@@ -74,13 +71,11 @@ StagingLayout layout_for(const std::vector<PoolInfo>& pools, const hicache_opts&
     per_page += int64_t(pi.T) * (all_layers ? pi.L : 1) * pi.P * pi.token_bytes;
   s.cap_pages = per_page > 0 ? int64_t(o.staging_bytes) / per_page : 0;
   int64_t off = 0;
-  s.vec16 = vec16_ok(pools) && aligned16(o.staging[0]) && aligned16(o.staging[1]);
   for (const PoolInfo& pi : pools) {
     std::vector<int64_t> offs;
     const int64_t region = s.cap_pages * (all_layers ? pi.L : 1) * pi.P * pi.token_bytes;
     for (int32_t t = 0; t < pi.T; ++t) {
       offs.push_back(off);
-      if (off % 16 != 0) s.vec16 = false;
       off += region;
     }
     s.region_off.push_back(offs);
@@ -91,17 +86,17 @@ StagingLayout layout_for(const std::vector<PoolInfo>& pools, const hicache_opts&
 SideSpec staging_side(const std::vector<PoolInfo>& pools, const StagingLayout& lay, char* base,
                       bool all_layers, int32_t layer_origin) {
   SideSpec side;
-  side.vec16 = lay.vec16;
   side.layer_origin = layer_origin;
   for (size_t p = 0; p < pools.size(); ++p) {
     const PoolInfo& pi = pools[p];
     std::vector<char*> b;
     for (int32_t t = 0; t < pi.T; ++t) b.push_back(base + lay.region_off[p][size_t(t)]);
-    side.base.push_back(b);
     const int64_t block = int64_t(pi.P) * pi.token_bytes;  // one (page, layer) block
     side.layer_stride.push_back(all_layers ? block : 0);
     side.page_stride.push_back(all_layers ? block * pi.L : block);
     side.paged_tokens.push_back(lay.cap_pages * pi.P);
+    side.vec16.push_back(vec16_ok(pi, b, side.layer_stride.back()));
+    side.base.push_back(b);
   }
   return side;
 }

@@ -20,6 +20,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <type_traits>
 #include <mutex>
 #include <string>
 
@@ -51,84 +52,174 @@ __device__ __forceinline__ uint32_t ld_stream(const uint32_t* p) { return __ldcs
 __device__ __forceinline__ void st_stream(uint4* p, const uint4& v) { __stcs(p, v); }
 __device__ __forceinline__ void st_stream(uint32_t* p, const uint32_t& v) { __stcs(p, v); }
 
-template <typename IdxT, int VEC, int MAXSEG>
+// Adds `count` finished tasks to burst layer `layer`; the warp that completes
+// the layer publishes its flag.  Called by all 32 lanes of a warp.
+template <int MAXSEG>
+__device__ __forceinline__ void flush_layer(const CopyParams<MAXSEG>& p, int layer,
+                                            uint32_t count, int lane) {
+  __threadfence();  // this lane's stores of the layer are visible device-wide
+  __syncwarp();
+  if (lane == 0) {
+    const int l = p.sig.layer_base + layer;
+    const uint32_t before = atomicAdd(&p.sig.done[l], count);
+    if (int64_t(before) + count == p.sig.tasks_per_layer) {
+      __threadfence();
+      atomicExch(&p.sig.flag[l], 1u);
+    }
+  }
+}
+
+// Copies the flat chunk range of one warp task.  offs[r] holds the source and
+// destination byte offsets of row r (x < 0 marks a skipped row); (r, j) is the
+// (row, chunk-in-row) position of chunk c0 + lane and advances by precomputed
+// quotients, so the loop has no division.
+template <typename V, int VEC>
+__device__ __forceinline__ void copy_chunks(const longlong2* offs, const char* src, char* dst,
+                                            const PoolGeom& g, int nr, int lane) {
+  const uint32_t cpr = g.cpr;
+  const uint32_t total = uint32_t(nr) * cpr;
+  uint32_t r = uint32_t(lane) / cpr;
+  uint32_t j = uint32_t(lane) - r * cpr;
+  for (uint32_t c0 = 0; c0 < total; c0 += 32u * kUnroll) {
+    V v[kUnroll];
+    int64_t dpos[kUnroll];
+    uint32_t rr = r, jj = j;
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      dpos[u] = -1;
+      if (c0 + uint32_t(lane) + 32u * u < total) {
+        const longlong2 o = offs[rr];
+        if (o.x >= 0) {
+          dpos[u] = o.y + int64_t(jj) * VEC;
+          v[u] = ld_stream(reinterpret_cast<const V*>(src + o.x + int64_t(jj) * VEC));
+        }
+      }
+      // advance by 32 chunks
+      jj += g.r32;
+      rr += g.q32;
+      if (jj >= cpr) { jj -= cpr; ++rr; }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u)
+      if (dpos[u] >= 0) st_stream(reinterpret_cast<V*>(dst + dpos[u]), v[u]);
+    // advance by 32 * kUnroll chunks
+    j += g.rS;
+    r += g.qS;
+    if (j >= cpr) { j -= cpr; ++r; }
+  }
+}
+
+// Copies the rows of one warp task and returns the task's launch-relative
+// segment.  Called by all 32 lanes of a warp; offs is the warp's table of
+// kMaxRowsPerTask entries in shared memory.
+template <typename IdxT, int MAXSEG>
+__device__ __forceinline__ int copy_task(const CopyParams<MAXSEG>& p, int64_t task, int lane,
+                                         longlong2* offs) {
+  // segment of this task: last s with seg_task_begin[s] <= task
+  int lo = 0, hi = p.nseg - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.seg_task_begin[mid] <= task) lo = mid; else hi = mid - 1;
+  }
+  const Segment sg = p.seg[lo];
+  const PoolGeom& g = p.pool[sg.pool];
+  const int64_t row0 = (task - p.seg_task_begin[lo]) * g.rows_per_task;
+  const int nr = int(min(int64_t(g.rows_per_task), g.nrows - row0));
+
+  // Each lane resolves rows lane, lane + 32, ... into byte offsets; all index
+  // loads are issued before any of them is used.
+  constexpr int kRowsPerLane = kMaxRowsPerTask / 32;
+  int64_t dv[kRowsPerLane], hv[kRowsPerLane];
+#pragma unroll
+  for (int q = 0; q < kRowsPerLane; ++q) {
+    const int r = lane + 32 * q;
+    if (r < nr) {
+      const int64_t pair = p.pair_begin + (row0 + r) * g.idx_stride;
+      dv[q] = load_index<IdxT>(p.dev_idx, pair);
+      hv[q] = p.paged_idx ? load_index<IdxT>(p.paged_idx, pair) : pair - p.pair_begin;
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < kRowsPerLane; ++q) {
+    const int r = lane + 32 * q;
+    if (r >= nr) break;
+    const int64_t d = dv[q];
+    const int64_t h = hv[q];
+    uint32_t e = 0;
+    if (d < 0 || d >= g.dev_tokens || h < 0 || h >= g.paged_tokens) {
+      e = HICACHE_DEVERR_RANGE;
+    } else if (g.idx_div > 1 && ((d % g.idx_div) != 0 || (h % g.idx_div) != 0)) {
+      e = HICACHE_DEVERR_PAGE_ALIGN;
+    }
+    longlong2 o = make_longlong2(-1, -1);
+    if (e != 0) {
+      if (p.err) atomicOr(p.err, e);
+    } else {
+      const uint32_t dr = uint32_t(d) / uint32_t(g.idx_div);
+      const uint32_t hr = uint32_t(h) / uint32_t(g.idx_div);
+      const uint32_t pg = hr / uint32_t(g.rows_per_page);
+      const uint32_t t = hr - pg * uint32_t(g.rows_per_page);
+      const int64_t doff = int64_t(dr) * g.row_bytes;
+      const int64_t poff = int64_t(pg) * g.paged_page_stride + int64_t(t) * g.row_bytes;
+      o = p.dir == kDevToPaged ? make_longlong2(doff, poff) : make_longlong2(poff, doff);
+    }
+    offs[r] = o;
+  }
+  __syncwarp();
+  const char* src = p.dir == kDevToPaged ? sg.dev : sg.paged;
+  char* dst = p.dir == kDevToPaged ? sg.paged : sg.dev;
+  if (g.vec == 16) copy_chunks<uint4, 16>(offs, src, dst, g, nr, lane);
+  else copy_chunks<uint32_t, 4>(offs, src, dst, g, nr, lane);
+  __syncwarp();  // the table is rewritten by the next task
+  return lo;
+}
+
+template <typename IdxT, int MAXSEG, bool SIGNAL>
 __global__ void __launch_bounds__(kThreadsPerCta)
     row_copy_kernel(const __grid_constant__ CopyParams<MAXSEG> p) {
-  using V = typename VecOf<VEC>::T;
+  __shared__ longlong2 row_offs[kWarpsPerCta][kMaxRowsPerTask];
   const int lane = threadIdx.x & 31;
-  const int64_t warps_total = int64_t(gridDim.x) * kWarpsPerCta;
+  longlong2* offs = row_offs[threadIdx.x >> 5];
   const int64_t ntasks = p.seg_task_begin[p.nseg];
-  for (int64_t task = int64_t(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5); task < ntasks;
-       task += warps_total) {
-    // segment of this task: last s with seg_task_begin[s] <= task
-    int lo = 0, hi = p.nseg - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (p.seg_task_begin[mid] <= task) lo = mid; else hi = mid - 1;
+  if constexpr (!SIGNAL) {
+    // Static striding: warp w takes tasks w, w + W, w + 2W, ...
+    const int64_t warps_total = int64_t(gridDim.x) * kWarpsPerCta;
+    for (int64_t task = int64_t(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5); task < ntasks;
+         task += warps_total)
+      copy_task<IdxT, MAXSEG>(p, task, lane, offs);
+  } else {
+    // Tasks are handed out in strict order from one counter, so every task of
+    // layer l is taken before any task of layer l+1 and a layer can only wait
+    // on the tasks still in flight when its last one was taken.  The next task
+    // is claimed before the current one is copied, hiding the atomic's latency.
+    uint32_t* next = p.sig.next + p.sig.layer_base;
+    int cur_layer = -1;    // launch-relative layer of the tasks counted in `pending`
+    uint32_t pending = 0;  // finished tasks of cur_layer not yet added to its counter
+    uint32_t claim = lane == 0 ? atomicAdd(next, 1u) : 0u;
+    int64_t task = __shfl_sync(0xffffffffu, claim, 0);
+    while (task < ntasks) {
+      claim = lane == 0 ? atomicAdd(next, 1u) : 0u;
+      const int layer = copy_task<IdxT, MAXSEG>(p, task, lane, offs) / p.sig.segs_per_layer;
+      if (layer != cur_layer) {
+        if (pending != 0) flush_layer(p, cur_layer, pending, lane);
+        cur_layer = layer;
+        pending = 0;
+      }
+      ++pending;
+      task = __shfl_sync(0xffffffffu, claim, 0);
     }
-    const Segment sg = p.seg[lo];
-    const PoolGeom& g = p.pool[sg.pool];
-    const int64_t row0 = (task - p.seg_task_begin[lo]) * g.rows_per_task;
-    const int nr = int(min(int64_t(g.rows_per_task), g.nrows - row0));
-
-    // Lane r < nr resolves row row0 + r into byte offsets (-1 marks a skipped row).
-    int64_t src_off = -1, dst_off = -1;
-    if (lane < nr) {
-      const int64_t pair = p.pair_begin + (row0 + lane) * g.idx_stride;
-      const int64_t d = load_index<IdxT>(p.dev_idx, pair);
-      const int64_t h = p.paged_idx ? load_index<IdxT>(p.paged_idx, pair) : pair - p.pair_begin;
-      uint32_t e = 0;
-      if (d < 0 || d >= g.dev_tokens || h < 0 || h >= g.paged_tokens) {
-        e = HICACHE_DEVERR_RANGE;
-      } else if (g.idx_div > 1 && ((d % g.idx_div) != 0 || (h % g.idx_div) != 0)) {
-        e = HICACHE_DEVERR_PAGE_ALIGN;
+    if (pending != 0) flush_layer(p, cur_layer, pending, lane);
+    // The last CTA to leave sets every flag of this launch's layers.  All tasks
+    // have been counted by then, so this only guarantees that no waiter can
+    // outlive the launch.
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      __threadfence();
+      const uint32_t gone = atomicAdd(&p.sig.exits[p.sig.layer_base], 1u);
+      if (gone == gridDim.x - 1) {
+        __threadfence();
+        for (int k = 0; k < p.sig.nlayers; ++k) atomicExch(&p.sig.flag[p.sig.layer_base + k], 1u);
       }
-      if (e != 0) {
-        if (p.err) atomicOr(p.err, e);
-      } else {
-        const uint32_t dr = uint32_t(d) / uint32_t(g.idx_div);
-        const uint32_t hr = uint32_t(h) / uint32_t(g.idx_div);
-        const uint32_t pg = hr / uint32_t(g.rows_per_page);
-        const uint32_t t = hr - pg * uint32_t(g.rows_per_page);
-        const int64_t doff = int64_t(dr) * g.row_bytes;
-        const int64_t poff = int64_t(pg) * g.paged_page_stride + int64_t(t) * g.row_bytes;
-        src_off = p.dir == kDevToPaged ? doff : poff;
-        dst_off = p.dir == kDevToPaged ? poff : doff;
-      }
-    }
-    const char* src = p.dir == kDevToPaged ? sg.dev : sg.paged;
-    char* dst = p.dir == kDevToPaged ? sg.paged : sg.dev;
-
-    // Flat chunk loop.  (r, j) = (row, chunk-in-row) of chunk c0 + lane.
-    const uint32_t cpr = g.cpr;
-    const uint32_t total = uint32_t(nr) * cpr;
-    uint32_t r = uint32_t(lane) / cpr;
-    uint32_t j = uint32_t(lane) - r * cpr;
-    for (uint32_t c0 = 0; c0 < total; c0 += 32u * kUnroll) {
-      V v[kUnroll];
-      int64_t dpos[kUnroll];
-      uint32_t rr = r, jj = j;
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const uint32_t c = c0 + uint32_t(lane) + 32u * u;
-        const int owner = int(min(rr, 31u));
-        const int64_t so = __shfl_sync(0xffffffffu, src_off, owner);
-        const int64_t dof = __shfl_sync(0xffffffffu, dst_off, owner);
-        const bool live = c < total && so >= 0;
-        dpos[u] = live ? dof + int64_t(jj) * VEC : -1;
-        if (live) v[u] = ld_stream(reinterpret_cast<const V*>(src + so + int64_t(jj) * VEC));
-        // advance by 32 chunks
-        jj += g.r32;
-        rr += g.q32;
-        if (jj >= cpr) { jj -= cpr; ++rr; }
-      }
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u)
-        if (dpos[u] >= 0) st_stream(reinterpret_cast<V*>(dst + dpos[u]), v[u]);
-      // advance by 32 * kUnroll chunks
-      j += g.rS;
-      r += g.qS;
-      if (j >= cpr) { j -= cpr; ++r; }
     }
   }
 }
@@ -156,20 +247,17 @@ hicache_status cuda_fail(cudaError_t e, const char* what) {
                                  cudaGetErrorString(e) + ")");
 }
 
-template <int MAXSEG>
-hicache_status launch_segments(const CopyParams<MAXSEG>& prm, int32_t index_bits, bool vec16,
-                               int64_t ntasks, const LaunchCfg& cfg, cudaStream_t stream) {
+template <int MAXSEG, bool SIGNAL>
+hicache_status launch_segments(const CopyParams<MAXSEG>& prm, int32_t index_bits, int64_t ntasks,
+                               const LaunchCfg& cfg, cudaStream_t stream) {
   if (ntasks <= 0) return HICACHE_OK;
   int max_ctas = cfg.max_ctas > 0 ? cfg.max_ctas : device_sm_count() * kDefaultCtasPerSm;
   const int64_t want = (ntasks + kWarpsPerCta - 1) / kWarpsPerCta;
   const int grid = int(std::max<int64_t>(1, std::min<int64_t>(want, max_ctas)));
-  if (index_bits == 32) {
-    if (vec16) row_copy_kernel<int32_t, 16, MAXSEG><<<grid, kThreadsPerCta, 0, stream>>>(prm);
-    else row_copy_kernel<int32_t, 4, MAXSEG><<<grid, kThreadsPerCta, 0, stream>>>(prm);
-  } else {
-    if (vec16) row_copy_kernel<int64_t, 16, MAXSEG><<<grid, kThreadsPerCta, 0, stream>>>(prm);
-    else row_copy_kernel<int64_t, 4, MAXSEG><<<grid, kThreadsPerCta, 0, stream>>>(prm);
-  }
+  if (index_bits == 32)
+    row_copy_kernel<int32_t, MAXSEG, SIGNAL><<<grid, kThreadsPerCta, 0, stream>>>(prm);
+  else
+    row_copy_kernel<int64_t, MAXSEG, SIGNAL><<<grid, kThreadsPerCta, 0, stream>>>(prm);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "row copy kernel launch");
   count_launch();
@@ -204,14 +292,12 @@ int64_t moved_row_bytes(const PoolInfo& pi) {
   return pi.page_granular ? pi.token_bytes * pi.P : pi.token_bytes;
 }
 
-bool vec16_ok(const std::vector<PoolInfo>& pools) {
-  for (const PoolInfo& pi : pools) {
-    if (moved_row_bytes(pi) % 16 != 0) return false;
-    for (char* ptr : pi.dev)
-      if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return false;
-    for (char* ptr : pi.host)
-      if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return false;
-  }
+bool vec16_ok(const PoolInfo& pi, const std::vector<char*>& paged_bases, int64_t layer_stride) {
+  if (moved_row_bytes(pi) % 16 != 0 || layer_stride % 16 != 0) return false;
+  for (char* ptr : pi.dev)
+    if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return false;
+  for (char* ptr : paged_bases)
+    if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return false;
   return true;
 }
 
@@ -226,24 +312,28 @@ void fill_geometry(const PoolInfo& pi, int64_t npairs, int vec, int64_t paged_pa
   g->idx_stride = pi.page_granular ? pi.P : 1;
   g->idx_div = pi.page_granular ? pi.P : 1;
   g->nrows = pi.page_granular ? npairs / pi.P : npairs;
+  g->vec = uint32_t(vec);
   g->cpr = uint32_t(R / vec);
   g->q32 = 32u / g->cpr;
   g->r32 = 32u % g->cpr;
   g->qS = uint32_t(32 * kUnroll) / g->cpr;
   g->rS = uint32_t(32 * kUnroll) % g->cpr;
-  const int64_t rpt = (int64_t(32) * kUnroll + g->cpr - 1) / g->cpr;
-  g->rows_per_task = int32_t(std::min<int64_t>(32, std::max<int64_t>(1, rpt)));
+  // about kTaskBytes per task: one row of 2 KiB, 128 rows of 16 B
+  const int64_t rpt = (kTaskBytes + R - 1) / R;
+  g->rows_per_task = int32_t(std::min<int64_t>(kMaxRowsPerTask, std::max<int64_t>(1, rpt)));
   g->tasks_per_seg = (g->nrows + g->rows_per_task - 1) / g->rows_per_task;
 }
 
 hicache_status launch_rows(const std::vector<PoolInfo>& pools, const SideSpec& side,
                            const void* dev_idx, const void* paged_idx, int32_t index_bits,
                            int64_t pair_begin, int64_t npairs, Dir dir, int32_t layer_begin,
-                           int32_t layer_end, const LaunchCfg& cfg, cudaStream_t stream) {
+                           int32_t layer_end, const LaunchCfg& cfg, cudaStream_t stream,
+                           const BurstWords* signal) {
   if (npairs <= 0 || layer_end <= layer_begin) return HICACHE_OK;
-  const bool vec16 = side.vec16;
-  const int vec = vec16 ? 16 : 4;
-  const bool small = int64_t(layer_end - layer_begin) * int64_t(pools.size()) * 2 <= kMaxSegSmall;
+  int32_t segs_per_layer = 0;
+  for (const PoolInfo& pi : pools) segs_per_layer += pi.T;
+  const bool small =
+      !signal && int64_t(layer_end - layer_begin) * segs_per_layer <= kMaxSegSmall;
 
   auto run = [&](auto& prm, int maxseg) -> hicache_status {
     prm.dev_idx = dev_idx;
@@ -251,11 +341,49 @@ hicache_status launch_rows(const std::vector<PoolInfo>& pools, const SideSpec& s
     prm.err = cfg.err;
     prm.dir = dir;
     prm.pair_begin = pair_begin;
-    for (size_t p = 0; p < pools.size(); ++p)
-      fill_geometry(pools[p], npairs, vec, side.page_stride[p], side.paged_tokens[p], &prm.pool[p]);
+    int64_t tasks_per_layer = 0;
+    for (size_t p = 0; p < pools.size(); ++p) {
+      fill_geometry(pools[p], npairs, side.vec16[p] ? 16 : 4, side.page_stride[p],
+                    side.paged_tokens[p], &prm.pool[p]);
+      tasks_per_layer += int64_t(pools[p].T) * prm.pool[p].tasks_per_seg;
+    }
+    // A signalling launch covers whole layers only, and counts a layer's tasks
+    // in one 32-bit word.
+    if (signal && tasks_per_layer >= (int64_t(1) << 32) - 1)
+      return fail(HICACHE_EINVAL, "single-launch burst: more than 2^32-2 tasks per layer");
+    const int cap = signal ? (maxseg / segs_per_layer) * segs_per_layer : maxseg;
     int nseg = 0;
     int64_t tasks = 0;
+    int32_t first_layer = layer_begin;
+    auto flush = [&](int32_t next_layer) -> hicache_status {
+      prm.nseg = nseg;
+      prm.seg_task_begin[nseg] = tasks;
+      hicache_status st;
+      if (signal) {
+        prm.sig.done = signal->done;
+        prm.sig.flag = signal->flag;
+        prm.sig.exits = signal->exits;
+        prm.sig.next = signal->next;
+        prm.sig.tasks_per_layer = tasks_per_layer;
+        prm.sig.segs_per_layer = segs_per_layer;
+        prm.sig.layer_base = first_layer - layer_begin;
+        prm.sig.nlayers = next_layer - first_layer;
+        st = launch_segments<std::remove_reference_t<decltype(prm)>::kMaxSeg, true>(
+            prm, index_bits, tasks, cfg, stream);
+      } else {
+        st = launch_segments<std::remove_reference_t<decltype(prm)>::kMaxSeg, false>(
+            prm, index_bits, tasks, cfg, stream);
+      }
+      nseg = 0;
+      tasks = 0;
+      first_layer = next_layer;
+      return st;
+    };
     for (int32_t l = layer_begin; l < layer_end; ++l) {
+      if (nseg + segs_per_layer > cap) {
+        const hicache_status st = flush(l);
+        if (st != HICACHE_OK) return st;
+      }
       for (size_t p = 0; p < pools.size(); ++p) {
         const PoolInfo& pi = pools[p];
         for (int32_t t = 0; t < pi.T; ++t) {
@@ -267,23 +395,10 @@ hicache_status launch_rows(const std::vector<PoolInfo>& pools, const SideSpec& s
           prm.seg_task_begin[nseg] = tasks;
           tasks += prm.pool[p].tasks_per_seg;
           ++nseg;
-          if (nseg == maxseg) {
-            prm.nseg = nseg;
-            prm.seg_task_begin[nseg] = tasks;
-            const hicache_status st = launch_segments(prm, index_bits, vec16, tasks, cfg, stream);
-            if (st != HICACHE_OK) return st;
-            nseg = 0;
-            tasks = 0;
-          }
         }
       }
     }
-    if (nseg > 0) {
-      prm.nseg = nseg;
-      prm.seg_task_begin[nseg] = tasks;
-      return launch_segments(prm, index_bits, vec16, tasks, cfg, stream);
-    }
-    return HICACHE_OK;
+    return nseg > 0 ? flush(layer_end) : HICACHE_OK;
   };
   if (small) {
     CopyParams<kMaxSegSmall> prm{};

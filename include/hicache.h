@@ -63,7 +63,7 @@
 extern "C" {
 #endif
 
-#define HICACHE_ABI_VERSION 1
+#define HICACHE_ABI_VERSION 2
 
 typedef enum hicache_status {
   HICACHE_OK = 0,
@@ -125,6 +125,10 @@ typedef struct hicache_opts {
   size_t staging_bytes;    /* bytes of each staging buffer */
   cudaStream_t copy_stream;/* staged path: stream for the DMA copies (0 = library-internal) */
   uint32_t* device_error;  /* optional device-accessible word; kernels OR HICACHE_DEVERR_* bits */
+  uint32_t* burst_words;   /* optional device memory of >= 4 words per burst layer: makes a
+                              zero-copy hicache_load_burst one kernel launch for all its layers
+                              (see hicache_load_burst); NULL = one launch per layer */
+  int64_t burst_words_len; /* number of uint32 words at burst_words */
 } hicache_opts;
 
 /*
@@ -160,14 +164,25 @@ hicache_status hicache_load_layer(const hicache_pool* pools, int32_t num_pools, 
                                   cudaStream_t stream, cudaEvent_t layer_done);
 
 /*
- * Load-back burst: layers layer_begin .. layer_end-1 in increasing order, each
- * followed by cudaEventRecord(layer_done[l - layer_begin], stream), so event l
- * means every pool's layer l has landed.  The indices are validated once for
- * the whole burst.  layer_done holds layer_end - layer_begin events (entries
- * may be NULL).  On any failure every non-NULL event is still recorded.
+ * Load-back burst: layers layer_begin .. layer_end-1 in increasing order; event
+ * layer_done[l - layer_begin] completes once every pool's layer l has landed.
+ * The indices are validated once for the whole burst.  layer_done holds
+ * layer_end - layer_begin events (entries may be NULL).  On any failure every
+ * non-NULL event is still recorded.
  * Passage: sglang PR #38472, Motivation (one burst of per-layer loads gated by
  * LayerDoneCounter.wait_until) and Modifications (failure completes every
  * layer event).
+ * Without opts->burst_words, each layer is one kernel launch on `stream`
+ * followed by cudaEventRecord(layer_done[...], stream).  With
+ * opts->burst_words (device memory, at least 4 * (layer_end - layer_begin)
+ * words, zeroed by the call itself), a zero-copy burst takes two launches: the
+ * first layer alone (its event recorded on `stream`), then one launch covering
+ * all other layers, its tasks handed out in layer order: the kernel sets one
+ * word per layer as the layer completes, a
+ * library stream forked from `stream` waits on each word with a stream memory
+ * wait and records the layer's event, and `stream` joins that stream before
+ * the call returns.  The words must not be shared by bursts that overlap on the
+ * GPU.  The staged path ignores burst_words.
  */
 hicache_status hicache_load_burst(const hicache_pool* pools, int32_t num_pools,
                                   int32_t layer_begin, int32_t layer_end,

@@ -37,11 +37,19 @@ def _staging(nbytes):
     return [torch.empty(nbytes, dtype=torch.uint8, device="cuda") for _ in range(2)]
 
 
+def _burst_words(layers):
+    """Device words for a single-launch burst (filled with junk: the call zeroes them)."""
+    return torch.full((4 * layers,), 12345, dtype=torch.int32, device="cuda")
+
+
+BURSTS = ["per_layer", "single_launch"]
+
+
 # ---------------------------------------------------------------- tiny MHA pool
 
 @pytest.mark.parametrize("where", ["device", "host"])
 @pytest.mark.parametrize("dtype", [torch.int32, torch.int64])
-@pytest.mark.parametrize("path", ["zero_copy", "staged"])
+@pytest.mark.parametrize("path", ["zero_copy", "staged", "zero_copy_single_launch"])
 def test_tiny_mha_backup_then_load(where, dtype, path):
     wl = W.tiny_mha()
     s = wl.pools[0]
@@ -56,6 +64,8 @@ def test_tiny_mha_backup_then_load(where, dtype, path):
         # room for 5 host pages of all layers: 64 pages take 13 chunks, both buffers alternate
         per_page = s.num_tensors * s.num_layers * s.page_size * s.row_bytes
         opts = _opts(hk.HICACHE_PATH_STAGED, where, staging=_staging(5 * per_page))
+    elif path == "zero_copy_single_launch":
+        opts = _opts(hk.HICACHE_PATH_ZERO_COPY, where, burst_words=_burst_words(s.num_layers))
     else:
         opts = _opts(hk.HICACHE_PATH_ZERO_COPY, where)
     hk.hicache_backup_all_layers(pool, dt, ht, opts=opts)
@@ -124,8 +134,10 @@ def test_ragged_backup_and_load(case, where):
     G.assert_device_equal(pool, dev1, "load")
 
 
-def test_grid_stride_and_many_segments():
-    """Three CTAs loop over many tasks; 600 segments need two launches of the all-layer kernel."""
+@pytest.mark.parametrize("burst", BURSTS)
+def test_grid_stride_and_many_segments(burst):
+    """Few CTAs loop over many tasks; 600 segments need two launches of the all-layer kernel,
+    and a single-launch burst of 280 two-tensor layers is cut into two launches."""
     s = G.shape(L=300, T=2, head_num=1, head_dim=8, dtype_size=2, P=4, slots=256, pages=40)
     pool = G.make_pool(s, seed=5)
     d, h = W.token_pairs(6, 150, 256, 160, 4, fragmented=True)
@@ -137,9 +149,13 @@ def test_grid_stride_and_many_segments():
     G.oracle_backup(pool, dev0, host0, d, h)
     G.assert_host_equal(pool, host0, "backup 600 segments")
     dev1 = G.device_images(pool)
-    hk.hicache_load_burst(pool, 10, 290, ht, dt, opts=_opts(hk.HICACHE_PATH_ZERO_COPY, "device",
-                                                            max_ctas=1))
+    words = _burst_words(280) if burst == "single_launch" else None
+    events = [torch.cuda.Event() for _ in range(280)]
+    hk.hicache_load_burst(pool, 10, 290, ht, dt, layer_done=events,
+                          opts=_opts(hk.HICACHE_PATH_ZERO_COPY, "device", max_ctas=1,
+                                     burst_words=words))
     torch.cuda.synchronize()
+    assert all(e.query() for e in events)
     G.oracle_load(pool, dev1, host0, range(10, 290), h, d)
     G.assert_device_equal(pool, dev1, "burst")
 
@@ -154,7 +170,7 @@ def _mla_dsa_shapes(L=5, P=64, pages=24, slots=64 * 40):
     return lat, idx
 
 
-@pytest.mark.parametrize("path", ["zero_copy", "staged"])
+@pytest.mark.parametrize("path", ["zero_copy", "staged", "zero_copy_single_launch"])
 def test_two_pools_mla_and_indexer(path):
     lat_s, idx_s = _mla_dsa_shapes()
     pools = [G.make_pool(lat_s, 7), G.make_pool(idx_s, 8)]
@@ -165,6 +181,9 @@ def test_two_pools_mla_and_indexer(path):
     if path == "staged":
         per_page = sum(p.num_layers * P * p.row_bytes for p in pools)
         opts = _opts(hk.HICACHE_PATH_STAGED, "host", staging=_staging(2 * per_page + 4096))
+    elif path == "zero_copy_single_launch":
+        opts = _opts(hk.HICACHE_PATH_ZERO_COPY, "host",
+                     burst_words=_burst_words(lat_s.num_layers))
     else:
         opts = _opts(hk.HICACHE_PATH_ZERO_COPY, "host")
     hk.hicache_backup_all_layers(pools, dt, ht, opts=opts)
@@ -247,6 +266,42 @@ def test_failed_burst_still_records_every_event():
     G.assert_device_equal(pool, dev0, "rejected burst moved bytes")
 
 
+def test_short_burst_words_rejected_and_events_recorded():
+    s = G.shape(L=4, T=1, head_num=1, head_dim=64, dtype_size=2, P=4, slots=256, pages=16)
+    pool = G.make_pool(s, 22)
+    dev0 = G.device_images(pool)
+    dt, ht = G.index_tensors([1, 2, 3], [5, 6, 7], "device")
+    events = [torch.cuda.Event() for _ in range(4)]
+    for e in events:
+        e.record()
+    torch.cuda.synchronize()
+    torch.cuda._sleep(200_000_000)
+    with pytest.raises(hk.HiCacheError) as ei:
+        hk.hicache_load_burst(pool, 0, 4, ht, dt, layer_done=events,
+                              opts=_opts(hk.HICACHE_PATH_ZERO_COPY, "device",
+                                         burst_words=_burst_words(3)))  # 12 words < 16
+    assert ei.value.status == hk.HICACHE_EINVAL
+    assert not any(e.query() for e in events)
+    torch.cuda.synchronize()
+    assert all(e.query() for e in events)
+    G.assert_device_equal(pool, dev0, "rejected burst moved bytes")
+
+
+def test_single_launch_burst_with_no_rows_completes_events():
+    """A page-granular pool with fewer pairs than one page moves nothing; events still fire."""
+    _, idx_s = _mla_dsa_shapes(L=3)
+    pool = G.make_pool(idx_s, 23)
+    dev0 = G.device_images(pool)
+    dt, ht = G.index_tensors(np.arange(10), np.arange(10), "device")
+    events = [torch.cuda.Event() for _ in range(3)]
+    hk.hicache_load_burst(pool, 0, 3, ht, dt, layer_done=events,
+                          opts=_opts(hk.HICACHE_PATH_ZERO_COPY, "device",
+                                     burst_words=_burst_words(3)))
+    torch.cuda.synchronize()
+    assert all(e.query() for e in events)
+    G.assert_device_equal(pool, dev0, "no rows")
+
+
 def test_duplicate_destination_rejected_and_nothing_moves():
     s = G.shape(L=2, T=1, head_num=1, head_dim=64, dtype_size=2, P=4, slots=256, pages=16)
     pool = G.make_pool(s, 16)
@@ -289,7 +344,8 @@ def test_empty_lists_record_events_and_move_nothing():
 
 # ----------------------------------------------------- events gate a consumer
 
-def test_layer_events_gate_consumer_checksum():
+@pytest.mark.parametrize("burst", BURSTS)
+def test_layer_events_gate_consumer_checksum(burst):
     """A consumer on another stream waits on event l only, and must see layer l fully loaded."""
     s = G.shape("mla", L=12, T=1, head_num=1, head_dim=576, dtype_size=2, P=64, slots=65536,
                 pages=512)
@@ -302,9 +358,10 @@ def test_layer_events_gate_consumer_checksum():
     consumer = torch.cuda.Stream()
     load_stream = torch.cuda.Stream()
     torch.cuda.synchronize()
+    opts = hk.Opts(burst_words=_burst_words(s.num_layers)) if burst == "single_launch" else None
     with torch.cuda.stream(load_stream):
         hk.hicache_load_burst(pool, 0, s.num_layers, ht, dt, layer_done=events,
-                              stream=load_stream)
+                              stream=load_stream, opts=opts)
     for l in range(s.num_layers):
         consumer.wait_event(events[l])
         hk.hicache_layer_checksum(pool, 0, l, dt, sums[l:l + 1], stream=consumer)
@@ -318,8 +375,9 @@ def test_layer_events_gate_consumer_checksum():
 
 # ------------------------------------------- full Llama-3-8B-shaped workload
 
-def test_llama3_8b_full_size_backup_and_burst():
-    """Full-size pools, the launch configuration the benchmark times; every byte compared."""
+@pytest.mark.parametrize("burst", BURSTS)
+def test_llama3_8b_full_size_backup_and_burst(burst):
+    """Full-size pools, the launch configurations the benchmark times; every byte compared."""
     wl = W.llama3_8b_mha()
     s = wl.pools[0]
     P = s.page_size
@@ -331,8 +389,9 @@ def test_llama3_8b_full_size_backup_and_burst():
     dt, ht = G.index_tensors(d, h, "device")
     d2t, _ = G.index_tensors(d2, h, "device")
     events = [torch.cuda.Event() for _ in range(s.num_layers)]
+    opts = hk.Opts(burst_words=_burst_words(s.num_layers)) if burst == "single_launch" else None
     hk.hicache_backup_all_layers(pool, dt, ht)
-    hk.hicache_load_burst(pool, 0, s.num_layers, ht, d2t, layer_done=events)
+    hk.hicache_load_burst(pool, 0, s.num_layers, ht, d2t, layer_done=events, opts=opts)
     torch.cuda.synchronize()
     G.oracle_backup(pool, dev0, host0, d, h)
     G.assert_host_equal(pool, host0, "full-size backup")
