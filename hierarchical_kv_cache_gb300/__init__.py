@@ -15,6 +15,8 @@ from ._binding import (  # noqa: F401
     HICACHE_ERANGE,
     HICACHE_INDEX_DEVICE,
     HICACHE_INDEX_HOST,
+    HICACHE_LAYOUT_PAGE_FIRST,
+    HICACHE_LAYOUT_PAGE_FIRST_DIRECT,
     HICACHE_OK,
     HICACHE_PATH_AUTO,
     HICACHE_PATH_STAGED,

@@ -24,6 +24,7 @@ STATUS_NAMES = {0: "HICACHE_OK", 1: "HICACHE_EINVAL", 2: "HICACHE_ERANGE", 3: "H
                 4: "HICACHE_EALIGN", 5: "HICACHE_ECUDA", 6: "HICACHE_ENOSTAGE"}
 HICACHE_PATH_AUTO, HICACHE_PATH_ZERO_COPY, HICACHE_PATH_STAGED = 0, 1, 2
 HICACHE_INDEX_HOST, HICACHE_INDEX_DEVICE = 0, 1
+HICACHE_LAYOUT_PAGE_FIRST_DIRECT, HICACHE_LAYOUT_PAGE_FIRST = 0, 1
 HICACHE_DEVERR_RANGE, HICACHE_DEVERR_PAGE_ALIGN = 1, 2
 
 
@@ -31,7 +32,7 @@ class c_pool(ctypes.Structure):
     _fields_ = [("num_layers", ctypes.c_int32), ("num_tensors", ctypes.c_int32),
                 ("head_num", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("dtype_size", ctypes.c_int32), ("page_size", ctypes.c_int32),
-                ("page_granular", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("page_granular", ctypes.c_int32), ("layout", ctypes.c_int32),
                 ("device_slots", ctypes.c_int64), ("host_pages", ctypes.c_int64),
                 ("device_layers", ctypes.POINTER(ctypes.c_void_p)),
                 ("host_tensors", ctypes.POINTER(ctypes.c_void_p))]
@@ -103,7 +104,8 @@ class Pool:
 
     Any tensor dtype works; the library sees bytes.  device_layers[t][l] must
     hold device_slots * row_bytes bytes and host_tensors[t] host_pages *
-    num_layers * page_size * row_bytes bytes.
+    num_layers * page_size * row_bytes bytes, in the host ``layout``
+    (HICACHE_LAYOUT_PAGE_FIRST_DIRECT or HICACHE_LAYOUT_PAGE_FIRST).
     """
 
     device_layers: Sequence[Sequence]
@@ -116,6 +118,7 @@ class Pool:
     device_slots: int
     host_pages: int
     page_granular: bool = False
+    layout: int = HICACHE_LAYOUT_PAGE_FIRST_DIRECT
     _keep: list = field(default_factory=list, repr=False)
 
     @property
@@ -135,7 +138,8 @@ class Pool:
         return c_pool(num_layers=L, num_tensors=T, head_num=self.head_num,
                       head_dim=self.head_dim, dtype_size=self.dtype_size,
                       page_size=self.page_size, page_granular=int(self.page_granular),
-                      reserved=0, device_slots=self.device_slots, host_pages=self.host_pages,
+                      layout=int(self.layout), device_slots=self.device_slots,
+                      host_pages=self.host_pages,
                       device_layers=ctypes.cast(dev, ctypes.POINTER(ctypes.c_void_p)),
                       host_tensors=ctypes.cast(host, ctypes.POINTER(ctypes.c_void_p)))
 

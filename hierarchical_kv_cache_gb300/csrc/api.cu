@@ -131,20 +131,6 @@ hicache_status check_burst_words(const hicache_opts& o, int32_t count) {
   return HICACHE_OK;
 }
 
-SideSpec host_side(const std::vector<PoolInfo>& pools) {
-  SideSpec s;
-  s.layer_origin = 0;
-  for (const PoolInfo& pi : pools) {
-    const int64_t layer_stride = int64_t(pi.P) * pi.token_bytes;
-    s.base.push_back(pi.host);
-    s.layer_stride.push_back(layer_stride);
-    s.page_stride.push_back(int64_t(pi.L) * pi.P * pi.token_bytes);
-    s.paged_tokens.push_back(pi.host_pages * pi.P);
-    s.vec16.push_back(vec16_ok(pi, pi.host, layer_stride));
-  }
-  return s;
-}
-
 LaunchCfg launch_cfg(const hicache_opts& o) { return LaunchCfg{o.max_ctas, o.device_error}; }
 
 hicache_path resolve_path(const Prepared& pr, Dir dir) {

@@ -93,6 +93,7 @@ struct CopyParams {
 struct PoolInfo {
   int32_t L, T, P;
   int32_t page_granular;
+  int32_t layout;           // hicache_layout of the host tensors
   int64_t token_bytes;      // R of one token row
   int64_t device_slots, host_pages;
   std::vector<char*> dev;   // T * L device layer pointers
@@ -144,14 +145,19 @@ struct SideSpec {
   std::vector<int64_t> layer_stride;      // [pool] bytes between layer blocks of one page
   std::vector<int64_t> page_stride;       // [pool] bytes between pages
   std::vector<int64_t> paged_tokens;      // [pool] token rows addressable on this side
+  std::vector<int32_t> rows_per_page;     // [pool] rows between page strides on this side
 };
 
+// True when the pool moves whole page rows (page-granular pool, direct layout).
+bool moves_page_rows(const PoolInfo& pi);
 int64_t moved_row_bytes(const PoolInfo& pi);
+// The host pool as a paged side, for either host layout.
+SideSpec host_side(const std::vector<PoolInfo>& pools);
 // 16-byte chunks are usable for pool `pi` against paged-side bases `paged_bases`
 // whose layer blocks are `layer_stride` bytes apart.
 bool vec16_ok(const PoolInfo& pi, const std::vector<char*>& paged_bases, int64_t layer_stride);
 void fill_geometry(const PoolInfo& pi, int64_t npairs, int vec, int64_t paged_page_stride,
-                   int64_t paged_tokens, PoolGeom* g);
+                   int64_t paged_tokens, int32_t rows_per_page, PoolGeom* g);
 // Moves pairs [pair_begin, pair_begin + npairs) for layers [layer_begin, layer_end)
 // of every pool and tensor between the device buffers and `side`.  With
 // `signal` (words of a single-launch burst: done, flag, exits, next, each

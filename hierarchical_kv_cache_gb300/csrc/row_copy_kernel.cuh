@@ -1,0 +1,227 @@
+// row_copy_kernel.cuh -- device code of the row-copy and checksum kernels.
+//
+// Included by zero_copy.cu only.  Kept in a file of its own so that a record of
+// hardware counters taken on these kernels can be tied to this exact code.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "hicache_internal.h"
+
+namespace hk {
+namespace {
+
+template <int VEC>
+struct VecOf;
+template <>
+struct VecOf<16> {
+  using T = uint4;
+};
+template <>
+struct VecOf<4> {
+  using T = uint32_t;
+};
+
+template <typename IdxT>
+__device__ __forceinline__ int64_t load_index(const void* base, int64_t i) {
+  return static_cast<int64_t>(static_cast<const IdxT*>(base)[i]);
+}
+
+// Streaming (evict-first) accesses: every byte is touched exactly once.
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) { return __ldcs(p); }
+__device__ __forceinline__ uint32_t ld_stream(const uint32_t* p) { return __ldcs(p); }
+__device__ __forceinline__ void st_stream(uint4* p, const uint4& v) { __stcs(p, v); }
+__device__ __forceinline__ void st_stream(uint32_t* p, const uint32_t& v) { __stcs(p, v); }
+
+// Adds `count` finished tasks to burst layer `layer`; the warp that completes
+// the layer publishes its flag.  Called by all 32 lanes of a warp.
+template <int MAXSEG>
+__device__ __forceinline__ void flush_layer(const CopyParams<MAXSEG>& p, int layer,
+                                            uint32_t count, int lane) {
+  __threadfence();  // this lane's stores of the layer are visible device-wide
+  __syncwarp();
+  if (lane == 0) {
+    const int l = p.sig.layer_base + layer;
+    const uint32_t before = atomicAdd(&p.sig.done[l], count);
+    if (int64_t(before) + count == p.sig.tasks_per_layer) {
+      __threadfence();
+      atomicExch(&p.sig.flag[l], 1u);
+    }
+  }
+}
+
+// Copies the flat chunk range of one warp task.  offs[r] holds the source and
+// destination byte offsets of row r (x < 0 marks a skipped row); (r, j) is the
+// (row, chunk-in-row) position of chunk c0 + lane and advances by precomputed
+// quotients, so the loop has no division.
+template <typename V, int VEC>
+__device__ __forceinline__ void copy_chunks(const longlong2* offs, const char* src, char* dst,
+                                            const PoolGeom& g, int nr, int lane) {
+  const uint32_t cpr = g.cpr;
+  const uint32_t total = uint32_t(nr) * cpr;
+  uint32_t r = uint32_t(lane) / cpr;
+  uint32_t j = uint32_t(lane) - r * cpr;
+  for (uint32_t c0 = 0; c0 < total; c0 += 32u * kUnroll) {
+    V v[kUnroll];
+    int64_t dpos[kUnroll];
+    uint32_t rr = r, jj = j;
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      dpos[u] = -1;
+      if (c0 + uint32_t(lane) + 32u * u < total) {
+        const longlong2 o = offs[rr];
+        if (o.x >= 0) {
+          dpos[u] = o.y + int64_t(jj) * VEC;
+          v[u] = ld_stream(reinterpret_cast<const V*>(src + o.x + int64_t(jj) * VEC));
+        }
+      }
+      // advance by 32 chunks
+      jj += g.r32;
+      rr += g.q32;
+      if (jj >= cpr) { jj -= cpr; ++rr; }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u)
+      if (dpos[u] >= 0) st_stream(reinterpret_cast<V*>(dst + dpos[u]), v[u]);
+    // advance by 32 * kUnroll chunks
+    j += g.rS;
+    r += g.qS;
+    if (j >= cpr) { j -= cpr; ++r; }
+  }
+}
+
+// Copies the rows of one warp task and returns the task's launch-relative
+// segment.  Called by all 32 lanes of a warp; offs is the warp's table of
+// kMaxRowsPerTask entries in shared memory.
+template <typename IdxT, int MAXSEG>
+__device__ __forceinline__ int copy_task(const CopyParams<MAXSEG>& p, int64_t task, int lane,
+                                         longlong2* offs) {
+  // segment of this task: last s with seg_task_begin[s] <= task
+  int lo = 0, hi = p.nseg - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.seg_task_begin[mid] <= task) lo = mid; else hi = mid - 1;
+  }
+  const Segment sg = p.seg[lo];
+  const PoolGeom& g = p.pool[sg.pool];
+  const int64_t row0 = (task - p.seg_task_begin[lo]) * g.rows_per_task;
+  const int nr = int(min(int64_t(g.rows_per_task), g.nrows - row0));
+
+  // Each lane resolves rows lane, lane + 32, ... into byte offsets; all index
+  // loads are issued before any of them is used.
+  constexpr int kRowsPerLane = kMaxRowsPerTask / 32;
+  int64_t dv[kRowsPerLane], hv[kRowsPerLane];
+#pragma unroll
+  for (int q = 0; q < kRowsPerLane; ++q) {
+    const int r = lane + 32 * q;
+    if (r < nr) {
+      const int64_t pair = p.pair_begin + (row0 + r) * g.idx_stride;
+      dv[q] = load_index<IdxT>(p.dev_idx, pair);
+      hv[q] = p.paged_idx ? load_index<IdxT>(p.paged_idx, pair) : pair - p.pair_begin;
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < kRowsPerLane; ++q) {
+    const int r = lane + 32 * q;
+    if (r >= nr) break;
+    const int64_t d = dv[q];
+    const int64_t h = hv[q];
+    uint32_t e = 0;
+    if (d < 0 || d >= g.dev_tokens || h < 0 || h >= g.paged_tokens) {
+      e = HICACHE_DEVERR_RANGE;
+    } else if (g.idx_div > 1 && ((d % g.idx_div) != 0 || (h % g.idx_div) != 0)) {
+      e = HICACHE_DEVERR_PAGE_ALIGN;
+    }
+    longlong2 o = make_longlong2(-1, -1);
+    if (e != 0) {
+      if (p.err) atomicOr(p.err, e);
+    } else {
+      const uint32_t dr = uint32_t(d) / uint32_t(g.idx_div);
+      const uint32_t hr = uint32_t(h) / uint32_t(g.idx_div);
+      const uint32_t pg = hr / uint32_t(g.rows_per_page);
+      const uint32_t t = hr - pg * uint32_t(g.rows_per_page);
+      const int64_t doff = int64_t(dr) * g.row_bytes;
+      const int64_t poff = int64_t(pg) * g.paged_page_stride + int64_t(t) * g.row_bytes;
+      o = p.dir == kDevToPaged ? make_longlong2(doff, poff) : make_longlong2(poff, doff);
+    }
+    offs[r] = o;
+  }
+  __syncwarp();
+  const char* src = p.dir == kDevToPaged ? sg.dev : sg.paged;
+  char* dst = p.dir == kDevToPaged ? sg.paged : sg.dev;
+  if (g.vec == 16) copy_chunks<uint4, 16>(offs, src, dst, g, nr, lane);
+  else copy_chunks<uint32_t, 4>(offs, src, dst, g, nr, lane);
+  __syncwarp();  // the table is rewritten by the next task
+  return lo;
+}
+
+template <typename IdxT, int MAXSEG, bool SIGNAL>
+__global__ void __launch_bounds__(kThreadsPerCta)
+    row_copy_kernel(const __grid_constant__ CopyParams<MAXSEG> p) {
+  __shared__ longlong2 row_offs[kWarpsPerCta][kMaxRowsPerTask];
+  const int lane = threadIdx.x & 31;
+  longlong2* offs = row_offs[threadIdx.x >> 5];
+  const int64_t ntasks = p.seg_task_begin[p.nseg];
+  if constexpr (!SIGNAL) {
+    // Static striding: warp w takes tasks w, w + W, w + 2W, ...
+    const int64_t warps_total = int64_t(gridDim.x) * kWarpsPerCta;
+    for (int64_t task = int64_t(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5); task < ntasks;
+         task += warps_total)
+      copy_task<IdxT, MAXSEG>(p, task, lane, offs);
+  } else {
+    // Tasks are handed out in strict order from one counter, so every task of
+    // layer l is taken before any task of layer l+1 and a layer can only wait
+    // on the tasks still in flight when its last one was taken.  The next task
+    // is claimed before the current one is copied, hiding the atomic's latency.
+    uint32_t* next = p.sig.next + p.sig.layer_base;
+    int cur_layer = -1;    // launch-relative layer of the tasks counted in `pending`
+    uint32_t pending = 0;  // finished tasks of cur_layer not yet added to its counter
+    uint32_t claim = lane == 0 ? atomicAdd(next, 1u) : 0u;
+    int64_t task = __shfl_sync(0xffffffffu, claim, 0);
+    while (task < ntasks) {
+      claim = lane == 0 ? atomicAdd(next, 1u) : 0u;
+      const int layer = copy_task<IdxT, MAXSEG>(p, task, lane, offs) / p.sig.segs_per_layer;
+      if (layer != cur_layer) {
+        if (pending != 0) flush_layer(p, cur_layer, pending, lane);
+        cur_layer = layer;
+        pending = 0;
+      }
+      ++pending;
+      task = __shfl_sync(0xffffffffu, claim, 0);
+    }
+    if (pending != 0) flush_layer(p, cur_layer, pending, lane);
+    // The last CTA to leave sets every flag of this launch's layers.  All tasks
+    // have been counted by then, so this only guarantees that no waiter can
+    // outlive the launch.
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      __threadfence();
+      const uint32_t gone = atomicAdd(&p.sig.exits[p.sig.layer_base], 1u);
+      if (gone == gridDim.x - 1) {
+        __threadfence();
+        for (int k = 0; k < p.sig.nlayers; ++k) atomicExch(&p.sig.flag[p.sig.layer_base + k], 1u);
+      }
+    }
+  }
+}
+
+// Synthetic consumer: sum of the 32-bit words of the rows at the given slots.
+template <typename IdxT>
+__global__ void __launch_bounds__(kThreadsPerCta)
+    checksum_kernel(const char* layer, int64_t row_bytes, const IdxT* idx, int64_t n,
+                    int64_t dev_slots, unsigned long long* out) {
+  unsigned long long acc = 0;
+  const int64_t words = row_bytes / 4;
+  for (int64_t i = blockIdx.x; i < n; i += gridDim.x) {
+    const int64_t d = static_cast<int64_t>(idx[i]);
+    if (d < 0 || d >= dev_slots) continue;
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(layer + d * row_bytes);
+    for (int64_t k = threadIdx.x; k < words; k += blockDim.x) acc += w[k];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_down_sync(0xffffffffu, acc, o);
+  if ((threadIdx.x & 31) == 0 && acc != 0) atomicAdd(out, acc);
+}
+
+}  // namespace
+}  // namespace hk

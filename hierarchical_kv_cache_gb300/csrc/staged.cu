@@ -92,8 +92,18 @@ SideSpec staging_side(const std::vector<PoolInfo>& pools, const StagingLayout& l
     std::vector<char*> b;
     for (int32_t t = 0; t < pi.T; ++t) b.push_back(base + lay.region_off[p][size_t(t)]);
     const int64_t block = int64_t(pi.P) * pi.token_bytes;  // one (page, layer) block
-    side.layer_stride.push_back(all_layers ? block : 0);
-    side.page_stride.push_back(all_layers ? block * pi.L : block);
+    const bool direct = pi.layout == HICACHE_LAYOUT_PAGE_FIRST_DIRECT;
+    if (all_layers && !direct) {
+      // backup staging mirrors a token-major host page: [token][layer][row]
+      side.layer_stride.push_back(pi.token_bytes);
+      side.page_stride.push_back(int64_t(pi.L) * pi.token_bytes);
+      side.rows_per_page.push_back(1);
+    } else {
+      // [page][layer][token][row] (backup), or one layer: [page][token][row] (load)
+      side.layer_stride.push_back(all_layers ? block : 0);
+      side.page_stride.push_back(all_layers ? block * pi.L : block);
+      side.rows_per_page.push_back(moves_page_rows(pi) ? 1 : pi.P);
+    }
     side.paged_tokens.push_back(lay.cap_pages * pi.P);
     side.vec16.push_back(vec16_ok(pi, b, side.layer_stride.back()));
     side.base.push_back(b);
@@ -231,17 +241,26 @@ hicache_status staged_load(const std::vector<PoolInfo>& pools, const hicache_opt
       if (step >= 2) HK_TRY(cudaStreamWaitEvent(copy, r->freed[b], 0), "cudaStreamWaitEvent(freed)");
       for (size_t p = 0; p < pools.size(); ++p) {
         const PoolInfo& pi = pools[p];
-        const int64_t block = int64_t(pi.P) * pi.token_bytes;  // one (page, layer) block
+        const int64_t R = pi.token_bytes;
+        const int64_t block = int64_t(pi.P) * R;  // one (page, layer) block
         const int64_t host_page = block * L;
+        const bool direct = pi.layout == HICACHE_LAYOUT_PAGE_FIRST_DIRECT;
         for (int32_t t = 0; t < pi.T; ++t) {
           for (int64_t j = g0; j < g1;) {
             int64_t e = j + 1;
             while (e < g1 && hp[size_t(e)] == hp[size_t(e - 1)] + 1) ++e;
-            const char* src = pi.host[size_t(t)] + hp[size_t(j)] * host_page + int64_t(l) * block;
             char* dst = side.base[p][size_t(t)] + (j - g0) * block;
-            HK_TRY(cudaMemcpy2DAsync(dst, size_t(block), src, size_t(host_page), size_t(block),
-                                     size_t(e - j), cudaMemcpyHostToDevice, copy),
-                   "cudaMemcpy2DAsync(host -> staging)");
+            const char* page0 = pi.host[size_t(t)] + hp[size_t(j)] * host_page;
+            // direct: one contiguous block per page, pages host_page apart;
+            // page_first: one row per token, tokens L * R apart
+            const cudaError_t ce =
+                direct ? cudaMemcpy2DAsync(dst, size_t(block), page0 + int64_t(l) * block,
+                                           size_t(host_page), size_t(block), size_t(e - j),
+                                           cudaMemcpyHostToDevice, copy)
+                       : cudaMemcpy2DAsync(dst, size_t(R), page0 + int64_t(l) * R,
+                                           size_t(L) * size_t(R), size_t(R),
+                                           size_t((e - j) * pi.P), cudaMemcpyHostToDevice, copy);
+            HK_TRY(ce, "cudaMemcpy2DAsync(host -> staging)");
             j = e;
           }
         }

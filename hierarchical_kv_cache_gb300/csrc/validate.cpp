@@ -58,7 +58,8 @@ hicache_status check_pools(const hicache_pool* pools, int32_t num_pools, std::ve
       return fail(HICACHE_EINVAL, who + "head_num, head_dim and dtype_size must be positive");
     if (q.page_size < 1) return fail(HICACHE_EINVAL, who + "page_size must be positive");
     if (q.page_granular != 0 && q.page_granular != 1) return fail(HICACHE_EINVAL, who + "page_granular must be 0 or 1");
-    if (q.reserved != 0) return fail(HICACHE_EINVAL, who + "reserved must be 0");
+    if (q.layout != HICACHE_LAYOUT_PAGE_FIRST_DIRECT && q.layout != HICACHE_LAYOUT_PAGE_FIRST)
+      return fail(HICACHE_EINVAL, who + "layout is not a hicache_layout");
     const int64_t R = int64_t(q.head_num) * q.head_dim * q.dtype_size;
     if (R > (int64_t(1) << 24)) return fail(HICACHE_EINVAL, who + "row bytes above 16 MiB");
     if (R % 4 != 0) return fail(HICACHE_EALIGN, who + "row bytes " + str(R) + " not a multiple of 4");
@@ -75,6 +76,7 @@ hicache_status check_pools(const hicache_pool* pools, int32_t num_pools, std::ve
     pi.T = q.num_tensors;
     pi.P = q.page_size;
     pi.page_granular = q.page_granular;
+    pi.layout = q.layout;
     pi.token_bytes = R;
     pi.device_slots = q.device_slots;
     pi.host_pages = q.host_pages;

@@ -21,7 +21,8 @@ def allocate_pool(shape, device: str = "cuda", pin_host: bool = True) -> Pool:
     return Pool(device_layers=dev, host_tensors=host, num_layers=L, head_num=shape.head_num,
                 head_dim=shape.head_dim, dtype_size=shape.dtype_size, page_size=shape.page_size,
                 device_slots=shape.device_slots, host_pages=shape.host_pages,
-                page_granular=bool(shape.page_granular))
+                page_granular=bool(shape.page_granular),
+                layout=1 if getattr(shape, "layout", "page_first_direct") == "page_first" else 0)
 
 
 def fill_device_random_(pool: Pool, seed: int, kind: str = "bf16_normal") -> None:

@@ -36,6 +36,7 @@ class PoolShape:
     host_pages: int
     page_granular: bool = False
     value_kind: str = "bf16_normal"  # or "uint8_uniform"
+    layout: str = "page_first_direct"  # host layout, or "page_first" (token-major)
 
     @property
     def row_bytes(self) -> int:

@@ -30,10 +30,15 @@
  *           byte ((h / P) * num_layers + l) * P * R + (h % P) * R of
  *           host_tensors[t].  One (page, layer) block is P * R contiguous bytes
  *           and one page holds the blocks of all layers in layer order.
+ *   That host order is HICACHE_LAYOUT_PAGE_FIRST_DIRECT (the default).  With
+ *   HICACHE_LAYOUT_PAGE_FIRST the host tensor is token-major instead, the shape
+ *   (token, layer, element) of the staging buffer in the sglang PR #28434
+ *   summary: host token h of layer l starts at byte (h * num_layers + l) * R.
+ *   Either way one host page (all layers) is P * num_layers * R contiguous bytes.
  *   A page-granular pool (DSA indexer-K: 128 fp8 values + one 4-byte scale per
  *   token) uses the same formulas; it only requires that the pairs cover whole,
- *   page-aligned pages, so that the library may move one P * R page row at a
- *   time even when R is not a multiple of 16.
+ *   page-aligned pages, so that with the direct layout the library may move one
+ *   P * R page row at a time even when R is not a multiple of 16.
  *
  * Ownership and ordering:
  *   The caller owns every pool, index array, staging buffer, stream and event;
@@ -96,6 +101,11 @@ typedef enum hicache_index_location {
   HICACHE_INDEX_DEVICE = 1
 } hicache_index_location;
 
+typedef enum hicache_layout {
+  HICACHE_LAYOUT_PAGE_FIRST_DIRECT = 0, /* host [page][layer][token][row] */
+  HICACHE_LAYOUT_PAGE_FIRST = 1         /* host [token][layer][row] (pages of P tokens) */
+} hicache_layout;
+
 /* Bits kernels OR into hicache_opts.device_error. */
 #define HICACHE_DEVERR_RANGE 1u     /* a pair was out of range and skipped */
 #define HICACHE_DEVERR_PAGE_ALIGN 2u /* a page-granular pair was not page-aligned and skipped */
@@ -108,11 +118,11 @@ typedef struct hicache_pool {
   int32_t dtype_size;     /* bytes per element (2 for bf16, 1 for uint8/fp8) */
   int32_t page_size;      /* P: tokens per page, the same for device and host */
   int32_t page_granular;  /* 1: pairs must cover whole page-aligned pages (DSA indexer) */
-  int32_t reserved;       /* must be 0 */
+  int32_t layout;         /* hicache_layout of the host tensors */
   int64_t device_slots;   /* token rows per device layer buffer */
   int64_t host_pages;     /* pages of the host pool */
   void* const* device_layers; /* host array of T * L device pointers, [t * L + l] */
-  void* const* host_tensors;  /* host array of T pinned host pointers (page-first) */
+  void* const* host_tensors;  /* host array of T pinned host pointers (see layout) */
 } hicache_pool;
 
 typedef struct hicache_opts {

@@ -15,10 +15,10 @@ from hierarchical_kv_cache_gb300.workloads import PoolShape
 
 
 def shape(name="p", L=4, T=2, head_num=2, head_dim=64, dtype_size=2, P=16, slots=4096, pages=512,
-          page_granular=False, value_kind="bf16_normal"):
+          page_granular=False, value_kind="bf16_normal", layout="page_first_direct"):
     return PoolShape(name, num_layers=L, num_tensors=T, head_num=head_num, head_dim=head_dim,
                      dtype_size=dtype_size, page_size=P, device_slots=slots, host_pages=pages,
-                     page_granular=page_granular, value_kind=value_kind)
+                     page_granular=page_granular, value_kind=value_kind, layout=layout)
 
 
 def make_pool(s: PoolShape, seed: int):
@@ -39,15 +39,23 @@ def host_images(pool):
 
 def oracle_backup(pool, dev_imgs, host_imgs, d, h):
     for t in range(pool.num_tensors):
-        oracle.backup_all_layers(dev_imgs[t], host_imgs[t], d, h, page_size=pool.page_size,
-                                 row_bytes=pool.row_bytes)
+        if pool.layout == 1:  # page_first, token-major
+            oracle.pf_backup_all_layers(dev_imgs[t], host_imgs[t], d, h, row_bytes=pool.row_bytes)
+        else:
+            oracle.backup_all_layers(dev_imgs[t], host_imgs[t], d, h, page_size=pool.page_size,
+                                     row_bytes=pool.row_bytes)
 
 
 def oracle_load(pool, dev_imgs, host_imgs, layers, h, d):
     for t in range(pool.num_tensors):
         for l in layers:
-            oracle.load_layer(dev_imgs[t][l], host_imgs[t], l, h, d, num_layers=pool.num_layers,
-                              page_size=pool.page_size, row_bytes=pool.row_bytes)
+            if pool.layout == 1:
+                oracle.pf_load_layer(dev_imgs[t][l], host_imgs[t], l, h, d,
+                                     num_layers=pool.num_layers, row_bytes=pool.row_bytes)
+            else:
+                oracle.load_layer(dev_imgs[t][l], host_imgs[t], l, h, d,
+                                  num_layers=pool.num_layers, page_size=pool.page_size,
+                                  row_bytes=pool.row_bytes)
 
 
 def assert_host_equal(pool, want_imgs, what=""):

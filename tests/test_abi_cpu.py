@@ -82,11 +82,11 @@ FAKE = 0x10000  # 64 KiB-aligned placeholder address, never dereferenced
 
 
 def c_pool(L=2, T=2, head_num=2, head_dim=8, dtype_size=2, P=4, slots=64, pages=8,
-           page_granular=0, dev_ptrs=None, host_ptrs=None):
+           page_granular=0, dev_ptrs=None, host_ptrs=None, layout=0):
     dev = (ctypes.c_void_p * (T * L))(*(dev_ptrs or [FAKE + 0x100000 * i for i in range(T * L)]))
     host = (ctypes.c_void_p * T)(*(host_ptrs or [FAKE + 0x10000000 * (i + 1) for i in range(T)]))
     p = B.c_pool(num_layers=L, num_tensors=T, head_num=head_num, head_dim=head_dim,
-                 dtype_size=dtype_size, page_size=P, page_granular=page_granular, reserved=0,
+                 dtype_size=dtype_size, page_size=P, page_granular=page_granular, layout=layout,
                  device_slots=slots, host_pages=pages,
                  device_layers=ctypes.cast(dev, ctypes.POINTER(ctypes.c_void_p)),
                  host_tensors=ctypes.cast(host, ctypes.POINTER(ctypes.c_void_p)))
@@ -132,6 +132,9 @@ def test_rejects_bad_pool_arguments():
     assert call_backup([c_pool(page_granular=1, slots=63)], [], []) == B.HICACHE_EINVAL
     o = B.c_opts(path=7)
     assert call_backup([c_pool()], [], [], opts=o) == B.HICACHE_EINVAL
+    assert call_backup([c_pool(layout=2)], [], []) == B.HICACHE_EINVAL
+    assert "layout" in err()
+    assert call_backup([c_pool(layout=1)], [], []) == B.HICACHE_OK
 
 
 def test_empty_call_is_ok_without_cuda():

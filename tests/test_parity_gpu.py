@@ -221,6 +221,79 @@ def test_indexer_rejects_partial_pages_on_device():
     G.assert_host_equal(pool, host0, "indexer aligned page only")
 
 
+# ------------------------------------------------------- page_first host layout
+
+@pytest.mark.parametrize("where", ["device", "host"])
+@pytest.mark.parametrize("path", ["zero_copy", "zero_copy_single_launch", "staged"])
+def test_page_first_layout_backup_then_load(where, path):
+    if path == "staged" and where == "device":
+        pytest.skip("the staged path plans DMA spans on the CPU: host-located indices only")
+    s = G.shape(L=5, T=2, head_num=2, head_dim=64, dtype_size=2, P=16, slots=4096, pages=96,
+                layout="page_first")
+    pool = G.make_pool(s, seed=24)
+    P = s.page_size
+    d, h, dp, _ = W.page_pairs(25, 40, s.device_slots // P, s.host_pages, P)
+    dev0, host0 = G.device_images(pool), G.host_images(pool)
+    dt, ht = G.index_tensors(d, h, where)
+    if path == "staged":
+        per_page = s.num_tensors * s.num_layers * P * s.row_bytes
+        opts = _opts(hk.HICACHE_PATH_STAGED, where, staging=_staging(3 * per_page))
+    elif path == "zero_copy_single_launch":
+        opts = _opts(hk.HICACHE_PATH_ZERO_COPY, where, burst_words=_burst_words(s.num_layers))
+    else:
+        opts = _opts(hk.HICACHE_PATH_ZERO_COPY, where)
+    hk.hicache_backup_all_layers(pool, dt, ht, opts=opts)
+    torch.cuda.synchronize()
+    G.oracle_backup(pool, dev0, host0, d, h)
+    G.assert_host_equal(pool, host0, "page_first backup")
+    d2, _, _, _ = W.page_pairs(26, 40, s.device_slots // P, s.host_pages, P,
+                               exclude_device_pages=dp)
+    d2t, _ = G.index_tensors(d2, h, where)
+    dev1 = G.device_images(pool)
+    events = [torch.cuda.Event() for _ in range(s.num_layers)]
+    hk.hicache_load_burst(pool, 0, s.num_layers, ht, d2t, opts=opts, layer_done=events)
+    torch.cuda.synchronize()
+    G.oracle_load(pool, dev1, host0, range(s.num_layers), h, d2)
+    G.assert_device_equal(pool, dev1, "page_first burst")
+
+
+@pytest.mark.parametrize("path", ["zero_copy", "zero_copy_single_launch", "staged"])
+def test_mixed_layouts_latent_direct_indexer_token_major(path):
+    """Latent pool page_first_direct (16-byte chunks) with an indexer pool in the token-major
+    layout (132-byte token rows, 4-byte chunks) in the same calls."""
+    lat = G.shape("mla", L=4, T=1, head_num=1, head_dim=576, dtype_size=2, P=64, slots=64 * 32,
+                  pages=20)
+    idx = G.shape("dsa", L=4, T=1, head_num=1, head_dim=132, dtype_size=1, P=64,
+                  slots=64 * 32, pages=20, page_granular=True, value_kind="uint8_uniform",
+                  layout="page_first")
+    pools = [G.make_pool(lat, 27), G.make_pool(idx, 28)]
+    P = 64
+    d, h, dp, _ = W.page_pairs(29, 7, 32, 20, P)
+    imgs = [(G.device_images(p), G.host_images(p)) for p in pools]
+    dt, ht = G.index_tensors(d, h, "host")
+    if path == "staged":
+        per_page = sum(p.num_layers * P * p.row_bytes for p in pools)
+        opts = _opts(hk.HICACHE_PATH_STAGED, "host", staging=_staging(3 * per_page))
+    elif path == "zero_copy_single_launch":
+        opts = _opts(hk.HICACHE_PATH_ZERO_COPY, "host", burst_words=_burst_words(4))
+    else:
+        opts = _opts(hk.HICACHE_PATH_ZERO_COPY, "host")
+    hk.hicache_backup_all_layers(pools, dt, ht, opts=opts)
+    torch.cuda.synchronize()
+    for p, (dev0, host0) in zip(pools, imgs):
+        G.oracle_backup(p, dev0, host0, d, h)
+        G.assert_host_equal(p, host0, "mixed-layout backup")
+    d2, _, _, _ = W.page_pairs(30, 7, 32, 20, P, exclude_device_pages=dp)
+    d2t, _ = G.index_tensors(d2, h, "host")
+    dev1s = [G.device_images(p) for p in pools]
+    hk.hicache_load_burst(pools, 0, 4, ht, d2t, opts=opts,
+                          layer_done=[torch.cuda.Event() for _ in range(4)])
+    torch.cuda.synchronize()
+    for p, dev1, (_, host0) in zip(pools, dev1s, imgs):
+        G.oracle_load(p, dev1, host0, range(4), h, d2)
+        G.assert_device_equal(p, dev1, "mixed-layout burst")
+
+
 # ----------------------------------------------------------------- error paths
 
 def test_device_indices_out_of_range_are_skipped_and_flagged():
