@@ -54,6 +54,8 @@ def parse_args():
     ap.add_argument("--burst", choices=["per_layer", "single_launch"], default="single_launch",
                     help="load burst as one kernel launch per layer, or one launch for all layers")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--consumer", action="store_true",
+                    help="also measure a consumer kernel gated by each layer event (config 3)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--out", default=None, help="also append the JSON line to this file")
@@ -92,13 +94,20 @@ def barrier(world):
 
 
 def max_over_ranks(x, world):
+    """Largest value of x over all ranks (NCCL on GPUs, gloo on CPU)."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def aggregate_gbs(world, steps, step_bytes, max_ms):
+    """Whole-job GB/s of `world` replicas that each moved steps * step_bytes, timed by the slowest."""
+    return world * steps * step_bytes / (max_ms * 1e-3) / GB
 
 
 # ---------------------------------------------------------------- clocks
@@ -346,10 +355,11 @@ def run_ours(args, rank, world):
     t_first = [ev_m[k].elapsed_time(ev_layers[k][0]) for k in range(K)]
     # layers 1..L-1 of a single-launch burst are one launch: first event to last event
     t_rest = [ev_layers[k][0].elapsed_time(ev_layers[k][-1]) for k in range(K)]
+    t_step = [ev_s[k].elapsed_time(ev_layers[k][-1]) for k in range(K)]
     per_layer = [ev_layers[k][l - 1].elapsed_time(ev_layers[k][l]) for k in range(K)
                  for l in range(1, L)]
     total_ms = max_over_ranks(total_ms, world)
-    value = world * K * step_bytes / (total_ms * 1e-3) / GB
+    value = aggregate_gbs(world, K, step_bytes, total_ms)
 
     mb, ml = statistics.mean(t_backup), statistics.mean(t_load)
     backup_gbs = bytes_backup / (mb * 1e-3) / GB
@@ -360,6 +370,10 @@ def run_ours(args, rank, world):
     # time-weighted link peak of the step's mix of directions
     peak_mix = step_bytes / (bytes_backup / link["d2h"] + bytes_load / link["h2d"])
     achieved = step_bytes / ((mb + ml) * 1e-3) / GB
+
+    consumer = None
+    if args.consumer:
+        consumer = run_consumer_overlap(hk, pools, idx_l, opts, L, stream, bytes_layer)
 
     e2e = None
     if not args.no_e2e:
@@ -392,6 +406,8 @@ def run_ours(args, rank, world):
             "first_layer_event_us": round(first_us, 1),
             "first_event_bound_us": round(bound_us, 1),
             "first_event_within_bound": first_us <= bound_us,
+            "step_ms_min_median_max": [round(min(t_step), 4), round(statistics.median(t_step), 4),
+                                       round(max(t_step), 4)],
             "enqueue_us_per_layer": round(statistics.median(enq_idle) * 1e6 / L, 2),
             "enqueue_us_per_layer_queue_full": round(statistics.median(enq) * 1e6 / L, 2),
             "link_peak_gbs": {k: round(v, 2) for k, v in link.items()},
@@ -428,6 +444,7 @@ def run_ours(args, rank, world):
         "gpu_launches": int(launches),
         "clocks": clk,
         "e2e": e2e,
+        "consumer_overlap": consumer,
         "wall_s_timed": round(wall, 3),
     }
     if args.burst == "single_launch" and args.path != "staged" and L > 1:
@@ -451,6 +468,62 @@ def run_ours(args, rank, world):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(wl, d, h, d2, args.cpu_seconds)
     return res
+
+
+def run_consumer_overlap(hk, pools, idx_l, opts, L, stream, bytes_layer, reps=5):
+    """Each layer's event gates a consumer kernel on another stream that reads that layer.
+
+    The consumer is the library's checksum kernel over the loaded rows of the
+    layer (every tensor of the first pool).  Reported: how long after its
+    layer's event each consumer finishes, and how much of the consumers' work is
+    hidden behind the burst (1.0 = all of it, 0.0 = none, as when every layer
+    lands before the forward starts).
+    """
+    import torch
+    cons = torch.cuda.Stream()
+    sums = torch.zeros(L, dtype=torch.int64, device="cuda")
+    pool0 = pools[0]
+    dev_idx = idx_l[1] if idx_l[1].is_cuda else idx_l[1].cuda()
+    hk.hicache_layer_checksum(pool0, 0, 0, dev_idx, sums[0:1], stream=cons)  # load the module
+    torch.cuda.synchronize()
+    lag, hidden, burst_ms, alone_ms = [], [], [], []
+    for _ in range(reps):
+        torch.cuda.synchronize()
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(L)]
+        done = [torch.cuda.Event(enable_timing=True) for _ in range(L)]
+        t0 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        cons.wait_stream(stream)
+        hk.hicache_load_burst(pools, 0, L, idx_l[0], idx_l[1], opts=opts, stream=stream,
+                              layer_done=evs)
+        for l in range(L):
+            cons.wait_event(evs[l])
+            for t in range(pool0.num_tensors):
+                hk.hicache_layer_checksum(pool0, t, l, dev_idx, sums[l:l + 1], stream=cons)
+            done[l].record(cons)
+        torch.cuda.synchronize()
+        lag.append(statistics.mean(evs[l].elapsed_time(done[l]) for l in range(L)) * 1e3)
+        burst = t0.elapsed_time(evs[-1])
+        total = t0.elapsed_time(done[-1])
+        # the consumers alone, back to back on loaded data
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record(cons)
+        for l in range(L):
+            for t in range(pool0.num_tensors):
+                hk.hicache_layer_checksum(pool0, t, l, dev_idx, sums[l:l + 1], stream=cons)
+        a1.record(cons)
+        torch.cuda.synchronize()
+        alone = a0.elapsed_time(a1)
+        burst_ms.append(burst)
+        alone_ms.append(alone)
+        hidden.append(max(0.0, min(1.0, (burst + alone - total) / alone)) if alone > 0 else None)
+    return {"consumer": "checksum kernel over each loaded layer, gated by that layer's event",
+            "mean_lag_after_event_us": round(statistics.median(lag), 1),
+            "burst_ms": round(statistics.median(burst_ms), 4),
+            "consumers_alone_ms": round(statistics.median(alone_ms), 4),
+            "fraction_of_consumer_work_hidden": round(statistics.median(hidden), 4),
+            "reps": reps}
 
 
 def run_e2e(hk, pools, wl, dt_h, ht_h, d2t_h, L, staging, path, args, step_bytes, n, words):

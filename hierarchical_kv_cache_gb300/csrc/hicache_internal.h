@@ -129,7 +129,10 @@ hicache_status plan_runs(const void* dev_idx, const void* host_idx, int32_t inde
                          int64_t* full_pages);
 
 // Launch-side helpers (zero_copy.cu).
-constexpr int kDefaultCtasPerSm = 2;
+// One 256-thread CTA per SM reaches the host-link peak in both directions on
+// GB300 and, next to a consumer kernel, keeps the same burst throughput as two
+// per SM while the consumer trails each layer event by half as long.
+constexpr int kDefaultCtasPerSm = 1;
 
 struct LaunchCfg {
   int max_ctas;   // 0 = default

@@ -226,7 +226,8 @@ hicache_status launch_checksum(const PoolInfo& pool, int32_t tensor, int32_t lay
                                cudaStream_t stream) {
   if (n <= 0) return HICACHE_OK;
   const char* base = pool.dev[size_t(tensor) * pool.L + layer];
-  const int grid = int(std::min<int64_t>(n, int64_t(device_sm_count()) * 4));
+  const int grid = int(std::min<int64_t>((n + kWarpsPerCta - 1) / kWarpsPerCta,
+                                         int64_t(device_sm_count()) * 4));
   auto* o = reinterpret_cast<unsigned long long*>(out);
   if (index_bits == 32)
     checksum_kernel<int32_t><<<grid, kThreadsPerCta, 0, stream>>>(

@@ -48,6 +48,10 @@
  *   before anything enqueued on `stream` after the call returns.  Index arrays,
  *   pools and staging buffers must stay valid until `stream` has passed the
  *   call.  Calls that share a staging buffer must be ordered by the caller.
+ *   On first use on a thread and device, the staged path and the single-launch
+ *   burst create one library stream and a few events there, kept until the
+ *   process exits; bursts issued from one thread share that stream, so their
+ *   layer events are recorded in issue order.
  *
  * Errors:
  *   Every function returns a hicache_status and never aborts or throws across

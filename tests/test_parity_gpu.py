@@ -294,6 +294,55 @@ def test_mixed_layouts_latent_direct_indexer_token_major(path):
         G.assert_device_equal(p, dev1, "mixed-layout burst")
 
 
+# ------------------------------------------------------- concurrent host threads
+
+def test_two_threads_burst_concurrently():
+    """Two host threads, each with its own stream, pool and burst words, run backups and
+    single-launch bursts at the same time; both results must match the oracle."""
+    import threading
+
+    s = G.shape("mla", L=6, T=1, head_num=1, head_dim=576, dtype_size=2, P=64, slots=64 * 64,
+                pages=48)
+    pools = [G.make_pool(s, 40 + k) for k in range(2)]
+    P = 64
+    pairs = [W.page_pairs(50 + k, 20, 64, 48, P) for k in range(2)]
+    fresh = [W.page_pairs(60 + k, 20, 64, 48, P, exclude_device_pages=pairs[k][2])[0]
+             for k in range(2)]
+    imgs = [(G.device_images(p), G.host_images(p)) for p in pools]
+    errors = []
+
+    def work(k):
+        try:
+            torch.cuda.set_device(0)
+            stream = torch.cuda.Stream()
+            d, h = pairs[k][0], pairs[k][1]
+            dt, ht = G.index_tensors(d, h, "host")
+            d2t, _ = G.index_tensors(fresh[k], h, "host")
+            opts = _opts(hk.HICACHE_PATH_ZERO_COPY, "host", burst_words=_burst_words(6))
+            for _ in range(3):
+                hk.hicache_backup_all_layers(pools[k], dt, ht, opts=opts, stream=stream)
+                hk.hicache_load_burst(pools[k], 0, 6, ht, d2t, opts=opts, stream=stream,
+                                      layer_done=[torch.cuda.Event() for _ in range(6)])
+            stream.synchronize()
+        except Exception as e:  # reported by the main thread
+            errors.append(repr(e))
+
+    threads = [threading.Thread(target=work, args=(k,)) for k in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    torch.cuda.synchronize()
+    for k, p in enumerate(pools):
+        dev0, host0 = imgs[k]
+        d, h = pairs[k][0], pairs[k][1]
+        G.oracle_backup(p, dev0, host0, d, h)
+        G.assert_host_equal(p, host0, f"thread {k} backup")
+        G.oracle_load(p, dev0, host0, range(6), h, fresh[k])
+        G.assert_device_equal(p, dev0, f"thread {k} burst")
+
+
 # ----------------------------------------------------------------- error paths
 
 def test_device_indices_out_of_range_are_skipped_and_flagged():
