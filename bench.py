@@ -356,6 +356,7 @@ def run_ours(args, rank, world):
     # layers 1..L-1 of a single-launch burst are one launch: first event to last event
     t_rest = [ev_layers[k][0].elapsed_time(ev_layers[k][-1]) for k in range(K)]
     t_step = [ev_s[k].elapsed_time(ev_layers[k][-1]) for k in range(K)]
+    k_med = sorted(range(K), key=lambda k: t_load[k])[K // 2]  # step with the median burst
     per_layer = [ev_layers[k][l - 1].elapsed_time(ev_layers[k][l]) for k in range(K)
                  for l in range(1, L)]
     total_ms = max_over_ranks(total_ms, world)
@@ -408,6 +409,10 @@ def run_ours(args, rank, world):
             "first_event_within_bound": first_us <= bound_us,
             "step_ms_min_median_max": [round(min(t_step), 4), round(statistics.median(t_step), 4),
                                        round(max(t_step), 4)],
+            "backup_ms_p50": round(statistics.median(t_backup), 4),
+            "load_burst_ms_p50": round(statistics.median(t_load), 4),
+            "layer_event_us_median_step": [round(ev_m[k_med].elapsed_time(e) * 1e3, 1)
+                                           for e in ev_layers[k_med]],
             "enqueue_us_per_layer": round(statistics.median(enq_idle) * 1e6 / L, 2),
             "enqueue_us_per_layer_queue_full": round(statistics.median(enq) * 1e6 / L, 2),
             "link_peak_gbs": {k: round(v, 2) for k, v in link.items()},

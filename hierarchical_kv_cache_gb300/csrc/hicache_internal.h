@@ -37,7 +37,7 @@ struct PoolGeom {
   int64_t dev_tokens;        // token rows of one device layer buffer (range check)
   int64_t paged_tokens;      // token rows of the paged side (range check)
   int64_t nrows;             // rows moved by one segment of this pool
-  int64_t tasks_per_seg;     // ceil(nrows / rows_per_task)
+  int64_t tasks_per_seg;     // ceil(nrows / rows_per_task), or nrows * parts_per_row
   int32_t rows_per_page;     // P for token pools, 1 for page-granular pools
   int32_t idx_stride;        // pair index of row k is k * idx_stride (P for page pools)
   int32_t idx_div;           // token index -> row index divisor (P for page pools)
@@ -46,6 +46,8 @@ struct PoolGeom {
   uint32_t q32, r32;         // 32 == q32 * cpr + r32
   uint32_t qS, rS;           // 32 * kUnroll == qS * cpr + rS
   uint32_t vec;              // chunk bytes: 16, or 4 when a row or base is not 16-aligned
+  int32_t parts_per_row;     // > 1: a row longer than a task is split into this many tasks
+  uint32_t part_chunks;      // chunks of one such part (the last part may be shorter)
 };
 
 // One (pool, tensor, layer) stream.

@@ -1,4 +1,4 @@
-// row_copy_kernel.cuh -- device code of the row-copy and checksum kernels.
+// row_copy_kernel.cuh -- device code of the row-copy kernel.
 //
 // Included by zero_copy.cu only.  Kept in a file of its own so that a record of
 // hardware counters taken on these kernels can be tied to this exact code.
@@ -50,17 +50,18 @@ __device__ __forceinline__ void flush_layer(const CopyParams<MAXSEG>& p, int lay
   }
 }
 
-// Copies the flat chunk range of one warp task.  offs[r] holds the source and
-// destination byte offsets of row r (x < 0 marks a skipped row); (r, j) is the
-// (row, chunk-in-row) position of chunk c0 + lane and advances by precomputed
-// quotients, so the loop has no division.
+// Copies the flat chunk range [chunk0, chunk0 + total) of one warp task, where
+// chunk c is chunk c % cpr of task row c / cpr.  offs[r] holds the source and
+// destination byte offsets of task row r (x < 0 marks a skipped row); (r, j)
+// is the (row, chunk-in-row) position of chunk chunk0 + c0 + lane and advances
+// by precomputed quotients, so the loop has no division.
 template <typename V, int VEC>
 __device__ __forceinline__ void copy_chunks(const longlong2* offs, const char* src, char* dst,
-                                            const PoolGeom& g, int nr, int lane) {
+                                            const PoolGeom& g, uint32_t chunk0, uint32_t total,
+                                            int lane) {
   const uint32_t cpr = g.cpr;
-  const uint32_t total = uint32_t(nr) * cpr;
-  uint32_t r = uint32_t(lane) / cpr;
-  uint32_t j = uint32_t(lane) - r * cpr;
+  uint32_t r = (chunk0 + uint32_t(lane)) / cpr;
+  uint32_t j = (chunk0 + uint32_t(lane)) - r * cpr;
   for (uint32_t c0 = 0; c0 < total; c0 += 32u * kUnroll) {
     V v[kUnroll];
     int64_t dpos[kUnroll];
@@ -104,8 +105,22 @@ __device__ __forceinline__ int copy_task(const CopyParams<MAXSEG>& p, int64_t ta
   }
   const Segment sg = p.seg[lo];
   const PoolGeom& g = p.pool[sg.pool];
-  const int64_t row0 = (task - p.seg_task_begin[lo]) * g.rows_per_task;
-  const int nr = int(min(int64_t(g.rows_per_task), g.nrows - row0));
+  // A task is rows_per_task whole rows, or one part of a row longer than a task.
+  const int64_t t = task - p.seg_task_begin[lo];
+  int64_t row0;
+  int nr;
+  uint32_t chunk0, total;
+  if (g.parts_per_row > 1) {
+    row0 = t / g.parts_per_row;
+    nr = 1;
+    chunk0 = uint32_t(t - row0 * g.parts_per_row) * g.part_chunks;
+    total = min(g.part_chunks, g.cpr - chunk0);
+  } else {
+    row0 = t * g.rows_per_task;
+    nr = int(min(int64_t(g.rows_per_task), g.nrows - row0));
+    chunk0 = 0;
+    total = uint32_t(nr) * g.cpr;
+  }
 
   // Each lane resolves rows lane, lane + 32, ... into byte offsets; all index
   // loads are issued before any of them is used.
@@ -149,8 +164,8 @@ __device__ __forceinline__ int copy_task(const CopyParams<MAXSEG>& p, int64_t ta
   __syncwarp();
   const char* src = p.dir == kDevToPaged ? sg.dev : sg.paged;
   char* dst = p.dir == kDevToPaged ? sg.paged : sg.dev;
-  if (g.vec == 16) copy_chunks<uint4, 16>(offs, src, dst, g, nr, lane);
-  else copy_chunks<uint32_t, 4>(offs, src, dst, g, nr, lane);
+  if (g.vec == 16) copy_chunks<uint4, 16>(offs, src, dst, g, chunk0, total, lane);
+  else copy_chunks<uint32_t, 4>(offs, src, dst, g, chunk0, total, lane);
   __syncwarp();  // the table is rewritten by the next task
   return lo;
 }
@@ -203,40 +218,6 @@ __global__ void __launch_bounds__(kThreadsPerCta)
       }
     }
   }
-}
-
-// Synthetic consumer: sum of the 32-bit words of the rows at the given slots.
-// One warp per row at a time; lanes read 16-byte chunks (4-byte words for a
-// row or base that is not 16-aligned), several chunks in flight per lane.
-template <typename IdxT>
-__global__ void __launch_bounds__(kThreadsPerCta)
-    checksum_kernel(const char* layer, int64_t row_bytes, const IdxT* idx, int64_t n,
-                    int64_t dev_slots, unsigned long long* out) {
-  const int lane = threadIdx.x & 31;
-  const int64_t warps_total = int64_t(gridDim.x) * kWarpsPerCta;
-  const bool vec16 = row_bytes % 16 == 0 && reinterpret_cast<uintptr_t>(layer) % 16 == 0;
-  unsigned long long acc = 0;
-  for (int64_t i = int64_t(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5); i < n;
-       i += warps_total) {
-    const int64_t d = static_cast<int64_t>(idx[i]);
-    if (d < 0 || d >= dev_slots) continue;
-    const char* row = layer + d * row_bytes;
-    if (vec16) {
-      const uint4* v = reinterpret_cast<const uint4*>(row);
-      const int64_t chunks = row_bytes / 16;
-#pragma unroll 4
-      for (int64_t k = lane; k < chunks; k += 32) {
-        const uint4 x = __ldcs(v + k);
-        acc += uint64_t(x.x) + x.y + x.z + x.w;
-      }
-    } else {
-      const uint32_t* w = reinterpret_cast<const uint32_t*>(row);
-      for (int64_t k = lane; k < row_bytes / 4; k += 32) acc += w[k];
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) acc += __shfl_down_sync(0xffffffffu, acc, o);
-  if (lane == 0 && acc != 0) atomicAdd(out, acc);
 }
 
 }  // namespace

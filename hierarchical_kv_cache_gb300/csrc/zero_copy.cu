@@ -24,6 +24,7 @@
 #include <mutex>
 #include <string>
 
+#include "consumer_kernel.cuh"
 #include "hicache_internal.h"
 #include "row_copy_kernel.cuh"
 
@@ -130,10 +131,15 @@ void fill_geometry(const PoolInfo& pi, int64_t npairs, int vec, int64_t paged_pa
   g->r32 = 32u % g->cpr;
   g->qS = uint32_t(32 * kUnroll) / g->cpr;
   g->rS = uint32_t(32 * kUnroll) % g->cpr;
-  // about kTaskBytes per task: one row of 2 KiB, 128 rows of 16 B
+  // about kTaskBytes per task: 128 rows of 16 B, one row of 2 KiB, or one
+  // 2 KiB part of a longer row (a state slot of several MiB, a long page row)
   const int64_t rpt = (kTaskBytes + R - 1) / R;
   g->rows_per_task = int32_t(std::min<int64_t>(kMaxRowsPerTask, std::max<int64_t>(1, rpt)));
-  g->tasks_per_seg = (g->nrows + g->rows_per_task - 1) / g->rows_per_task;
+  g->part_chunks = uint32_t(kTaskBytes / vec);
+  g->parts_per_row = R > kTaskBytes ? int32_t((g->cpr + g->part_chunks - 1) / g->part_chunks) : 1;
+  g->tasks_per_seg = g->parts_per_row > 1
+                         ? g->nrows * g->parts_per_row
+                         : (g->nrows + g->rows_per_task - 1) / g->rows_per_task;
 }
 
 hicache_status launch_rows(const std::vector<PoolInfo>& pools, const SideSpec& side,

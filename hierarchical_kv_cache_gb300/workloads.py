@@ -92,11 +92,34 @@ def mla78_dsa() -> Workload:
                                 "layer events, plus an all-layer backup of 1024 pages")
 
 
+def mamba_state() -> Workload:
+    """Hybrid-model state pools: per-request conv and SSM state slots of the Mamba layers.
+
+    The pages list MambaPoolHost among the host pools with staged write-back
+    ("[HiCache] Support hybrid-pool staged write-back JIT kernel", implementation
+    breakdown) without printing their shapes; these follow a Mamba-2 layer with
+    d_inner 4096, 8 groups, d_state 128, d_conv 4 and 64 heads of 64: the conv
+    state holds 2*4096 + 2*8*128 = 10240 channels x 3 bf16 taps (60 KiB per slot
+    and layer), the SSM state 64 x 64 x 128 fp32 values (2 MiB).  A slot is one
+    request, so page_size is 1 and a row is a whole state.
+    """
+    conv = PoolShape("mamba_conv", num_layers=24, num_tensors=1, head_num=10240, head_dim=3,
+                     dtype_size=2, page_size=1, device_slots=64, host_pages=128)
+    ssm = PoolShape("mamba_ssm", num_layers=24, num_tensors=1, head_num=64, head_dim=64 * 128,
+                    dtype_size=4, page_size=1, device_slots=64, host_pages=128,
+                    value_kind="uint8_uniform")
+    return Workload("hybrid-model Mamba state pools (24 layers, conv 60 KiB + SSM 2 MiB per "
+                    "slot, page_size 1)", (conv, ssm), move_pages=32, seed=5,
+                    description="all-layer backup of 32 request slots, then a load-back burst "
+                                "of those slots to fresh device slots with 24 layer events")
+
+
 WORKLOADS = {
     "tiny_mha": tiny_mha,
     "llama3_8b_mha": llama3_8b_mha,
     "dsv3_mla": dsv3_mla,
     "mla78_dsa": mla78_dsa,
+    "mamba_state": mamba_state,
 }
 
 SWEEP_ROW_BYTES = (16, 64, 256, 1152, 2048)

@@ -294,6 +294,43 @@ def test_mixed_layouts_latent_direct_indexer_token_major(path):
         G.assert_device_equal(p, dev1, "mixed-layout burst")
 
 
+# ------------------------------------------------- hybrid-model state pools (P=1)
+
+@pytest.mark.parametrize("path", ["zero_copy", "zero_copy_single_launch", "staged"])
+def test_state_pools_with_multi_mib_rows(path):
+    """Mamba-style conv (60 KiB) and SSM (2 MiB) state slots: rows far longer than one warp
+    task, split into parts; two pools of different row sizes in one call."""
+    conv = G.shape("conv", L=3, T=1, head_num=10240, head_dim=3, dtype_size=2, P=1, slots=16,
+                   pages=24)
+    ssm = G.shape("ssm", L=3, T=1, head_num=64, head_dim=64 * 128, dtype_size=4, P=1,
+                  slots=16, pages=24, value_kind="uint8_uniform")
+    pools = [G.make_pool(conv, 70), G.make_pool(ssm, 71)]
+    d, h, dp, _ = W.page_pairs(72, 7, 16, 24, 1)
+    imgs = [(G.device_images(p), G.host_images(p)) for p in pools]
+    dt, ht = G.index_tensors(d, h, "host")
+    if path == "staged":
+        per_slot = sum(p.num_layers * p.row_bytes for p in pools)
+        opts = _opts(hk.HICACHE_PATH_STAGED, "host", staging=_staging(3 * per_slot))
+    elif path == "zero_copy_single_launch":
+        opts = _opts(hk.HICACHE_PATH_ZERO_COPY, "host", burst_words=_burst_words(3))
+    else:
+        opts = _opts(hk.HICACHE_PATH_ZERO_COPY, "host")
+    hk.hicache_backup_all_layers(pools, dt, ht, opts=opts)
+    torch.cuda.synchronize()
+    for p, (dev0, host0) in zip(pools, imgs):
+        G.oracle_backup(p, dev0, host0, d, h)
+        G.assert_host_equal(p, host0, "state backup")
+    d2, _, _, _ = W.page_pairs(73, 7, 16, 24, 1, exclude_device_pages=dp)
+    d2t, _ = G.index_tensors(d2, h, "host")
+    dev1s = [G.device_images(p) for p in pools]
+    hk.hicache_load_burst(pools, 0, 3, ht, d2t, opts=opts,
+                          layer_done=[torch.cuda.Event() for _ in range(3)])
+    torch.cuda.synchronize()
+    for p, dev1, (_, host0) in zip(pools, dev1s, imgs):
+        G.oracle_load(p, dev1, host0, range(3), h, d2)
+        G.assert_device_equal(p, dev1, "state burst")
+
+
 # ------------------------------------------------------- concurrent host threads
 
 def test_two_threads_burst_concurrently():
