@@ -54,6 +54,8 @@ def parse_args():
     ap.add_argument("--burst", choices=["per_layer", "single_launch"], default="single_launch",
                     help="load burst as one kernel launch per layer, or one launch for all layers")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--duplex", action="store_true",
+                    help="also measure backup and load-back running concurrently (full duplex)")
     ap.add_argument("--consumer", action="store_true",
                     help="also measure a consumer kernel gated by each layer event (config 3)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -168,6 +170,82 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- host link peak
+
+def measure_duplex_peak(nbytes=1 << 30, reps=3):
+    """Pinned DMA in both directions at once (two streams), best of `reps`: GB/s of both."""
+    import torch
+    h1 = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    h2 = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    d1 = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    d2 = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    best = 0.0
+    for r in range(reps + 1):
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(sa)
+        sb.wait_event(e0)
+        with torch.cuda.stream(sa):
+            h1.copy_(d1, non_blocking=True)
+        with torch.cuda.stream(sb):
+            d2.copy_(h2, non_blocking=True)
+        sa.wait_stream(sb)
+        e1.record(sa)
+        e1.synchronize()
+        if r:
+            best = max(best, 2 * nbytes / (e0.elapsed_time(e1) * 1e-3) / GB)
+    del h1, h2, d1, d2
+    torch.cuda.synchronize()
+    return best
+
+
+def run_duplex(hk, pools, wl, idx_b, L, opts_b, opts_l, n, reps=10):
+    """Backup on one stream and a load burst of other host pages on another, concurrently.
+
+    Write-back of newly computed KV and load-back of cache hits are independent
+    in a serving system; the host link is full duplex.  The load reads host
+    pages the backup does not write and fills device slots the backup does not
+    read.
+    """
+    import torch
+    from hierarchical_kv_cache_gb300 import workloads as W
+    s0 = wl.pools[0]
+    P = s0.page_size
+    dev_pages = min(s.device_slots for s in wl.pools) // P
+    host_pages = min(s.host_pages for s in wl.pools)
+    d_b = idx_b[0].cpu().numpy()
+    h_b = idx_b[1].cpu().numpy()
+    g = W.rng(wl.seed + 77)
+    hp = W.sample_pages(g, host_pages, wl.move_pages, exclude=np.unique(h_b // P))
+    dp = W.sample_pages(g, dev_pages, wl.move_pages, exclude=np.unique(d_b // P))
+    h_l = torch.as_tensor(W.expand_pages(hp, P)).cuda()
+    d_l = torch.as_tensor(W.expand_pages(dp, P)).cuda()
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    evs = [torch.cuda.Event() for _ in range(L)]
+    bytes_backup, bytes_layer = payload_bytes(wl, n)
+    peak = measure_duplex_peak()
+    times = []
+    for r in range(reps + 2):
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(sa)
+        sb.wait_event(e0)
+        hk.hicache_backup_all_layers(pools, idx_b[0], idx_b[1], opts=opts_b, stream=sa)
+        hk.hicache_load_burst(pools, 0, L, h_l, d_l, opts=opts_l, stream=sb, layer_done=evs)
+        sa.wait_stream(sb)
+        e1.record(sa)
+        e1.synchronize()
+        if r >= 2:
+            times.append(e0.elapsed_time(e1))
+    ms = statistics.median(times)
+    gbs = (bytes_backup + bytes_layer * L) / (ms * 1e-3) / GB
+    return {"what": "all-layer backup and a load-back burst of other host pages, concurrently "
+                    "on two streams",
+            "gbs": round(gbs, 2), "ms": round(ms, 4), "duplex_dma_peak_gbs": round(peak, 2),
+            "frac_of_duplex_dma_peak": round(gbs / peak, 4), "reps": reps}
+
 
 def measure_link_peak(nbytes=1 << 30, reps=5):
     import torch
@@ -372,6 +450,14 @@ def run_ours(args, rank, world):
     peak_mix = step_bytes / (bytes_backup / link["d2h"] + bytes_load / link["h2d"])
     achieved = step_bytes / ((mb + ml) * 1e-3) / GB
 
+    duplex = None
+    if args.duplex and args.path != "staged":
+        words2 = (torch.zeros(4 * L, dtype=torch.int32, device="cuda")
+                  if args.burst == "single_launch" else None)
+        opts_l = hk.Opts(path=path, index_location=hk.HICACHE_INDEX_DEVICE,
+                         max_ctas=args.max_ctas, device_error=err, burst_words=words2)
+        duplex = run_duplex(hk, pools, wl, idx_b, L, opts, opts_l, n)
+
     consumer = None
     if args.consumer:
         consumer = run_consumer_overlap(hk, pools, idx_l, opts, L, stream, bytes_layer)
@@ -450,6 +536,7 @@ def run_ours(args, rank, world):
         "clocks": clk,
         "e2e": e2e,
         "consumer_overlap": consumer,
+        "duplex": duplex,
         "wall_s_timed": round(wall, 3),
     }
     if args.burst == "single_launch" and args.path != "staged" and L > 1:

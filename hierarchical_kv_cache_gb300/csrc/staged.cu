@@ -158,7 +158,7 @@ hicache_status staged_backup(const std::vector<PoolInfo>& pools, const hicache_o
   st = get_res(&r);
   if (st != HICACHE_OK) return st;
   cudaStream_t copy = o.copy_stream ? o.copy_stream : r->copy;
-  const LaunchCfg cfg{o.max_ctas, o.device_error};
+  const LaunchCfg cfg{o.max_ctas, o.device_error, /*paged_in_hbm=*/true};
   const int64_t groups = int64_t(hp.size());
   const SideSpec side[2] = {staging_side(pools, lay, static_cast<char*>(o.staging[0]), true, 0),
                             staging_side(pools, lay, static_cast<char*>(o.staging[1]), true, 0)};
@@ -219,7 +219,7 @@ hicache_status staged_load(const std::vector<PoolInfo>& pools, const hicache_opt
   st = get_res(&r);
   if (st != HICACHE_OK) return finish(0, st);
   cudaStream_t copy = o.copy_stream ? o.copy_stream : r->copy;
-  const LaunchCfg cfg{o.max_ctas, o.device_error};
+  const LaunchCfg cfg{o.max_ctas, o.device_error, /*paged_in_hbm=*/true};
   const int64_t groups = int64_t(hp.size());
 
 #define HK_TRY(call, what)                                    \

@@ -41,7 +41,9 @@ template <int MAXSEG, bool SIGNAL>
 hicache_status launch_segments(const CopyParams<MAXSEG>& prm, int32_t index_bits, int64_t ntasks,
                                const LaunchCfg& cfg, cudaStream_t stream) {
   if (ntasks <= 0) return HICACHE_OK;
-  int max_ctas = cfg.max_ctas > 0 ? cfg.max_ctas : device_sm_count() * kDefaultCtasPerSm;
+  const int per_sm = cfg.paged_in_hbm ? kCtasPerSmHbm
+                     : prm.dir == kDevToPaged ? kCtasPerSmToHost : kCtasPerSmFromHost;
+  const int max_ctas = cfg.max_ctas > 0 ? cfg.max_ctas : device_sm_count() * per_sm;
   const int64_t want = (ntasks + kWarpsPerCta - 1) / kWarpsPerCta;
   const int grid = int(std::max<int64_t>(1, std::min<int64_t>(want, max_ctas)));
   if (index_bits == 32)
