@@ -34,4 +34,13 @@ from ._binding import (  # noqa: F401
     kernel_launches,
     lib,
 )
-from .pools import allocate_pool  # noqa: F401
+
+
+def __getattr__(name):
+    # torch is only needed for pool allocation; import it on first use so that
+    # the binding and the workload generators load without it.
+    if name == "allocate_pool":
+        from .pools import allocate_pool
+
+        return allocate_pool
+    raise AttributeError(name)
