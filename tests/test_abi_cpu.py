@@ -137,6 +137,24 @@ def test_rejects_bad_pool_arguments():
     assert call_backup([c_pool(layout=1)], [], []) == B.HICACHE_OK
 
 
+def test_limits_are_rejected_just_beyond_the_maxima():
+    assert call_backup([c_pool(L=4097)], [], []) == B.HICACHE_EINVAL  # 4096 layers at most
+    assert call_backup([c_pool(L=4096)], [], []) == B.HICACHE_OK
+    # rows of at most 16 MiB: 2 x 4 Mi x 2 B = 16 MiB passes, one more head does not
+    assert call_backup([c_pool(head_num=2, head_dim=4 << 20, dtype_size=2)], [], []) == B.HICACHE_OK
+    assert call_backup([c_pool(head_num=3, head_dim=4 << 20, dtype_size=2)], [], []) == B.HICACHE_EINVAL
+    assert call_backup([c_pool(slots=(1 << 31))], [], []) == B.HICACHE_EINVAL
+    assert call_backup([c_pool(pages=(1 << 29), P=4)], [], []) == B.HICACHE_EINVAL
+    lib = B.lib()
+    arr = (B.c_pool * 1)(c_pool())
+    d = np.zeros(4, dtype=np.int64)
+    assert lib.hicache_backup_all_layers(arr, 1, d.ctypes.data, d.ctypes.data, 64, 1 << 31, None,
+                                         None) == B.HICACHE_EINVAL
+    assert "2^31" in err()
+    assert lib.hicache_backup_all_layers(arr, 5, d.ctypes.data, d.ctypes.data, 64, 0, None,
+                                         None) == B.HICACHE_EINVAL  # at most 4 pools
+
+
 def test_empty_call_is_ok_without_cuda():
     assert call_backup([c_pool()], [], []) == B.HICACHE_OK
     assert call_load([c_pool()], 1, [], []) == B.HICACHE_OK

@@ -160,6 +160,54 @@ def test_grid_stride_and_many_segments(burst):
     G.assert_device_equal(pool, dev1, "burst")
 
 
+@pytest.mark.parametrize("burst", BURSTS)
+def test_maximum_layer_count(burst):
+    """4096 layers (the most a pool may have) x 2 tensors: 8192 segments, so the backup takes 16
+    all-layer launches and the single-launch burst is cut into 16 signalling launches."""
+    L = 4096
+    s = G.shape(L=L, T=2, head_num=1, head_dim=8, dtype_size=2, P=2, slots=64, pages=16)
+    pool = G.make_pool(s, seed=80)
+    d, h = W.token_pairs(81, 12, 64, 32, 2, fragmented=True)
+    dev0, host0 = G.device_images(pool), G.host_images(pool)
+    dt, ht = G.index_tensors(d, h, "device")
+    hk.hicache_backup_all_layers(pool, dt, ht, opts=_opts(hk.HICACHE_PATH_ZERO_COPY, "device"))
+    torch.cuda.synchronize()
+    G.oracle_backup(pool, dev0, host0, d, h)
+    G.assert_host_equal(pool, host0, "4096-layer backup")
+    d2 = np.setdiff1d(np.arange(64), d)[:12]
+    d2t, _ = G.index_tensors(d2, h, "device")
+    dev1 = G.device_images(pool)
+    words = _burst_words(L) if burst == "single_launch" else None
+    events = [torch.cuda.Event() for _ in range(L)]
+    hk.hicache_load_burst(pool, 0, L, ht, d2t, layer_done=events,
+                          opts=_opts(hk.HICACHE_PATH_ZERO_COPY, "device", burst_words=words))
+    torch.cuda.synchronize()
+    assert all(e.query() for e in events)
+    G.oracle_load(pool, dev1, host0, range(L), h, d2)
+    G.assert_device_equal(pool, dev1, "4096-layer burst")
+
+
+def test_maximum_row_size():
+    """Rows of 16 MiB (the most a row may hold), page_size 1: 8192 part-tasks per row."""
+    s = G.shape(L=2, T=1, head_num=2, head_dim=4 << 20, dtype_size=2, P=1, slots=4, pages=4,
+                value_kind="uint8_uniform")
+    pool = G.make_pool(s, seed=82)
+    d, h = np.array([3, 0], dtype=np.int64), np.array([1, 2], dtype=np.int64)
+    dev0, host0 = G.device_images(pool), G.host_images(pool)
+    dt, ht = G.index_tensors(d, h, "host")
+    hk.hicache_backup_all_layers(pool, dt, ht)
+    torch.cuda.synchronize()
+    G.oracle_backup(pool, dev0, host0, d, h)
+    G.assert_host_equal(pool, host0, "16 MiB rows backup")
+    d2, _ = G.index_tensors(np.array([1, 2], dtype=np.int64), h, "host")
+    dev1 = G.device_images(pool)
+    hk.hicache_load_burst(pool, 0, 2, ht, d2, opts=hk.Opts(burst_words=_burst_words(2)),
+                          layer_done=[torch.cuda.Event(), torch.cuda.Event()])
+    torch.cuda.synchronize()
+    G.oracle_load(pool, dev1, host0, range(2), h, np.array([1, 2], dtype=np.int64))
+    G.assert_device_equal(pool, dev1, "16 MiB rows burst")
+
+
 # ------------------------------------------------------- MLA + DSA indexer pools
 
 def _mla_dsa_shapes(L=5, P=64, pages=24, slots=64 * 40):
