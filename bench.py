@@ -623,8 +623,10 @@ def run_e2e(hk, pools, wl, dt_h, ht_h, d2t_h, L, staging, path, args, step_bytes
     import torch
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     err_h = torch.zeros(1, dtype=torch.int32).pin_memory()
+    idx_staging = torch.empty(hk.index_staging_bytes(n, 64), dtype=torch.uint8, device="cuda")
     opts = hk.Opts(path=path, index_location=hk.HICACHE_INDEX_HOST, staging=staging,
-                   max_ctas=args.max_ctas, device_error=err, burst_words=words)
+                   max_ctas=args.max_ctas, device_error=err, burst_words=words,
+                   index_staging=idx_staging)
     events = [torch.cuda.Event() for _ in range(L)]
     stream = torch.cuda.Stream()
 
@@ -651,7 +653,8 @@ def run_e2e(hk, pools, wl, dt_h, ht_h, d2t_h, L, staging, path, args, step_bytes
             "h2d_bytes_per_step": int(bytes_layer * L + idx_bytes),
             "d2h_bytes_per_step": int(bytes_backup + 4),
             "note": "host wall clock per step; pinned host indices validated on the CPU each "
-                    "call; payload crosses the host link by definition of the op"}
+                    "call and copied by the library into opts.index_staging; payload crosses "
+                    "the host link by definition of the op"}
 
 
 # ---------------------------------------------------------------- CPU oracle

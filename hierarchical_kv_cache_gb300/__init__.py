@@ -31,6 +31,7 @@ from ._binding import (  # noqa: F401
     hicache_load_burst,
     hicache_load_layer,
     hicache_plan_runs,
+    index_staging_bytes,
     kernel_launches,
     lib,
 )

@@ -43,7 +43,8 @@ class c_opts(ctypes.Structure):
                 ("max_ctas", ctypes.c_int32), ("reserved", ctypes.c_int32),
                 ("staging", ctypes.c_void_p * 2), ("staging_bytes", ctypes.c_size_t),
                 ("copy_stream", ctypes.c_void_p), ("device_error", ctypes.c_void_p),
-                ("burst_words", ctypes.c_void_p), ("burst_words_len", ctypes.c_int64)]
+                ("burst_words", ctypes.c_void_p), ("burst_words_len", ctypes.c_int64),
+                ("index_staging", ctypes.c_void_p), ("index_staging_bytes", ctypes.c_size_t)]
 
 
 class c_run(ctypes.Structure):
@@ -82,6 +83,8 @@ def lib():
         L.hicache_abi_version.argtypes = []
         L.hicache_kernel_launches.restype = ctypes.c_int64
         L.hicache_kernel_launches.argtypes = []
+        L.hicache_index_staging_bytes.restype = ctypes.c_size_t
+        L.hicache_index_staging_bytes.argtypes = [i64, i32]
         _lib = L
     return _lib
 
@@ -155,6 +158,7 @@ class Opts:
     copy_stream: Optional[object] = None  # torch.cuda.Stream
     device_error: Optional[object] = None  # int32/uint32 tensor of one element
     burst_words: Optional[object] = None  # int32 CUDA tensor, >= 4 words per burst layer
+    index_staging: Optional[object] = None  # CUDA tensor for copies of host-located indices
 
 
 def _pools_arg(pools):
@@ -191,6 +195,9 @@ def _opts_arg(opts: Optional[Opts], a, b):
     if o.burst_words is not None:
         c.burst_words = o.burst_words.data_ptr()
         c.burst_words_len = o.burst_words.numel() * o.burst_words.element_size() // 4
+    if o.index_staging is not None:
+        c.index_staging = o.index_staging.data_ptr()
+        c.index_staging_bytes = o.index_staging.numel() * o.index_staging.element_size()
     return c
 
 
@@ -309,6 +316,11 @@ def hicache_layer_checksum(pool: Pool, tensor: int, layer: int, device_indices, 
 
 def abi_version() -> int:
     return lib().hicache_abi_version()
+
+
+def index_staging_bytes(n: int, index_bits: int = 64) -> int:
+    """Bytes of Opts.index_staging a call with n pairs needs."""
+    return lib().hicache_index_staging_bytes(n, index_bits)
 
 
 def kernel_launches() -> int:

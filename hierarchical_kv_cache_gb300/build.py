@@ -46,7 +46,7 @@ def _compile_cmd(src: str, obj: str, ptxas_verbose: bool):
         if ptxas_verbose:
             cmd += ["-Xptxas", "-v"]
         return cmd
-    return ["g++", "-c", src, "-o", obj, "-std=c++17", "-O2", "-fPIC", "-Wall", "-Wextra", *inc]
+    return ["g++", "-c", src, "-o", obj, "-std=c++17", "-O3", "-fPIC", "-Wall", "-Wextra", *inc]
 
 
 def up_to_date() -> bool:

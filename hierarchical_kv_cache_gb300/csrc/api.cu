@@ -70,6 +70,33 @@ struct Prepared {
 };
 
 // Checks arguments and indices; resolves device-visible addresses.
+size_t index_array_bytes(int64_t n, int32_t bits) {
+  return (size_t(n) * size_t(bits / 8) + 15) / 16 * 16;
+}
+
+// With host-located indices and opts.index_staging, copies both validated index
+// arrays into the staging buffer on `stream` and points the kernels at the copies.
+hicache_status stage_indices(Prepared* pr, cudaStream_t stream) {
+  const hicache_opts& o = pr->o;
+  if (o.index_location != HICACHE_INDEX_HOST || !o.index_staging || pr->idx.n == 0)
+    return HICACHE_OK;
+  const size_t one = index_array_bytes(pr->idx.n, pr->idx.bits);
+  if (o.index_staging_bytes < 2 * one)
+    return fail(HICACHE_EINVAL, "opts.index_staging holds " + std::to_string(o.index_staging_bytes) +
+                                    " bytes; this call needs " + std::to_string(2 * one));
+  if (reinterpret_cast<uintptr_t>(o.index_staging) % 16 != 0)
+    return fail(HICACHE_EALIGN, "opts.index_staging is not 16-byte aligned");
+  char* dst = static_cast<char*>(o.index_staging);
+  const size_t bytes = size_t(pr->idx.n) * size_t(pr->idx.bits / 8);
+  cudaError_t e = cudaMemcpyAsync(dst, pr->idx.dev_cpu, bytes, cudaMemcpyHostToDevice, stream);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(dst + one, pr->idx.host_cpu, bytes, cudaMemcpyHostToDevice, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync(indices -> opts.index_staging)");
+  pr->idx.dev_gpu = dst;
+  pr->idx.host_gpu = dst + one;
+  return HICACHE_OK;
+}
+
 // When check_layers is set, [layer_begin, layer_end) must lie inside the pools' layers.
 hicache_status prepare(const hicache_pool* pools, int32_t num_pools, const void* dev_idx,
                        const void* host_idx, int32_t bits, int64_t n, const hicache_opts* opts,
@@ -188,6 +215,8 @@ extern "C" hicache_status hicache_backup_all_layers(const hicache_pool* pools, i
   hicache_status st = prepare(pools, num_pools, device_indices, host_indices, index_bits, n, opts,
                               /*dest_is_device=*/false, false, 0, 0, &pr);
   if (st != HICACHE_OK || n == 0) return st;
+  st = stage_indices(&pr, stream);
+  if (st != HICACHE_OK) return st;
   const hicache_path path = resolve_path(pr, kDevToPaged);
   if (path == HICACHE_PATH_STAGED)
     return staged_backup(pr.pools, pr.o, pr.idx, stream);
@@ -205,6 +234,7 @@ extern "C" hicache_status hicache_load_layer(const hicache_pool* pools, int32_t 
   Prepared pr;
   hicache_status st = prepare(pools, num_pools, device_indices, host_indices, index_bits, n, opts,
                               /*dest_is_device=*/true, true, layer, layer + 1, &pr);
+  if (st == HICACHE_OK && n > 0) st = stage_indices(&pr, stream);
   if (st != HICACHE_OK || n == 0) {
     record_events(evs, 1, stream);
     return st;
@@ -224,6 +254,7 @@ extern "C" hicache_status hicache_load_burst(const hicache_pool* pools, int32_t 
   hicache_status st = prepare(pools, num_pools, device_indices, host_indices, index_bits, n, opts,
                               /*dest_is_device=*/true, true, layer_begin, layer_end, &pr);
   if (st == HICACHE_OK) st = check_burst_words(pr.o, count);
+  if (st == HICACHE_OK && n > 0) st = stage_indices(&pr, stream);
   if (st != HICACHE_OK || n == 0) {
     record_events(layer_done, count, stream);
     return st;
@@ -338,6 +369,11 @@ extern "C" hicache_status hicache_layer_checksum(const hicache_pool* pool, int32
 }
 
 extern "C" int64_t hicache_kernel_launches(void) { return kernel_launches(); }
+
+extern "C" size_t hicache_index_staging_bytes(int64_t n, int32_t index_bits) {
+  if (n <= 0 || (index_bits != 32 && index_bits != 64)) return 0;
+  return 2 * index_array_bytes(n, index_bits);
+}
 
 extern "C" const char* hicache_last_error(void) { return last_error().c_str(); }
 

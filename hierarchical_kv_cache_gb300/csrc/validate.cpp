@@ -31,6 +31,37 @@ inline int64_t idx(const void* p, int32_t bits, int64_t i) {
 std::string str(int64_t v) { return std::to_string(v); }
 
 constexpr int64_t kMaxRows = (int64_t(1) << 31) - 1;
+
+template <typename T>
+void min_max(const T* p, int64_t n, int64_t* mn, int64_t* mx) {
+  T lo = p[0], hi = p[0];
+  for (int64_t i = 1; i < n; ++i) {
+    lo = p[i] < lo ? p[i] : lo;
+    hi = p[i] > hi ? p[i] : hi;
+  }
+  *mn = int64_t(lo);
+  *mx = int64_t(hi);
+}
+
+// Sets one bit per value (all in range); returns the index of the first value
+// seen twice, or -1.  Leaves the bitmap all zero again either way.
+template <typename T>
+int64_t mark_distinct(const T* p, int64_t n, uint64_t* bitmap) {
+  int64_t dup = -1, upto = n;
+  for (int64_t i = 0; i < n; ++i) {
+    const uint64_t x = uint64_t(p[i]);
+    const uint64_t bit = uint64_t(1) << (x & 63);
+    uint64_t& w = bitmap[x >> 6];
+    if (w & bit) {
+      dup = i;
+      upto = i;
+      break;
+    }
+    w |= bit;
+  }
+  for (int64_t i = 0; i < upto; ++i) bitmap[uint64_t(p[i]) >> 6] = 0;
+  return dup;
+}
 }  // namespace
 
 hicache_status check_whole_pages(bool any_page, int64_t P, const void* dev_idx, const void* host_idx,
@@ -127,14 +158,26 @@ hicache_status check_pairs_host(const std::vector<PoolInfo>& pools, const void* 
     host_lim = std::min(host_lim, p.host_pages * int64_t(p.P));
     any_page = any_page || p.page_granular;
   }
-  // Range: every pair must address a row of every pool of the call.
-  for (int64_t i = 0; i < n; ++i) {
-    const int64_t d = idx(dev_idx, bits, i);
-    const int64_t h = idx(host_idx, bits, i);
-    if (d < 0 || d >= dev_lim)
-      return fail(HICACHE_ERANGE, "device index " + str(d) + " at pair " + str(i) + " outside [0, " + str(dev_lim) + ")");
-    if (h < 0 || h >= host_lim)
-      return fail(HICACHE_ERANGE, "host index " + str(h) + " at pair " + str(i) + " outside [0, " + str(host_lim) + ")");
+  // Range: every pair must address a row of every pool of the call.  A
+  // min/max pass (which the compiler vectorises) decides; only a failing call
+  // walks the pairs again to name the first offender.
+  int64_t dmin, dmax, hmin, hmax;
+  if (bits == 32) {
+    min_max(static_cast<const int32_t*>(dev_idx), n, &dmin, &dmax);
+    min_max(static_cast<const int32_t*>(host_idx), n, &hmin, &hmax);
+  } else {
+    min_max(static_cast<const int64_t*>(dev_idx), n, &dmin, &dmax);
+    min_max(static_cast<const int64_t*>(host_idx), n, &hmin, &hmax);
+  }
+  if (dmin < 0 || dmax >= dev_lim || hmin < 0 || hmax >= host_lim) {
+    for (int64_t i = 0; i < n; ++i) {
+      const int64_t d = idx(dev_idx, bits, i);
+      const int64_t h = idx(host_idx, bits, i);
+      if (d < 0 || d >= dev_lim)
+        return fail(HICACHE_ERANGE, "device index " + str(d) + " at pair " + str(i) + " outside [0, " + str(dev_lim) + ")");
+      if (h < 0 || h >= host_lim)
+        return fail(HICACHE_ERANGE, "host index " + str(h) + " at pair " + str(i) + " outside [0, " + str(host_lim) + ")");
+    }
   }
   // Distinct destinations: a bitmap over the destination rows, cleared again
   // after use so that the cost stays O(n) per call.
@@ -154,22 +197,13 @@ hicache_status check_pairs_host(const std::vector<PoolInfo>& pools, const void* 
   static thread_local std::vector<uint64_t> bitmap;
   const size_t words = size_t((lim + 63) / 64);
   if (bitmap.size() < words) bitmap.assign(words, 0);
-  hicache_status st = HICACHE_OK;
-  int64_t set_upto = n;
-  for (int64_t i = 0; i < n; ++i) {
-    const int64_t x = idx(dst, bits, i);
-    uint64_t& w = bitmap[size_t(x >> 6)];
-    const uint64_t bit = uint64_t(1) << (x & 63);
-    if (w & bit) {
-      st = fail(HICACHE_EDUP, std::string(dest_is_device ? "device" : "host") + " destination " + str(x) +
-                                  " named twice (second time at pair " + str(i) + ")");
-      set_upto = i;
-      break;
-    }
-    w |= bit;
-  }
-  for (int64_t i = 0; i < set_upto; ++i) bitmap[size_t(idx(dst, bits, i) >> 6)] = 0;
-  if (st != HICACHE_OK) return st;
+  const int64_t first_dup = bits == 32
+      ? mark_distinct(static_cast<const int32_t*>(dst), n, bitmap.data())
+      : mark_distinct(static_cast<const int64_t*>(dst), n, bitmap.data());
+  if (first_dup >= 0)
+    return fail(HICACHE_EDUP, std::string(dest_is_device ? "device" : "host") + " destination " +
+                                  str(idx(dst, bits, first_dup)) + " named twice (second time at pair " +
+                                  str(first_dup) + ")");
   return check_whole_pages(any_page, P, dev_idx, host_idx, bits, n);
 }
 

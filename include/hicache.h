@@ -72,7 +72,7 @@
 extern "C" {
 #endif
 
-#define HICACHE_ABI_VERSION 2
+#define HICACHE_ABI_VERSION 3
 
 typedef enum hicache_status {
   HICACHE_OK = 0,
@@ -143,6 +143,11 @@ typedef struct hicache_opts {
                               zero-copy hicache_load_burst one kernel launch for all its layers
                               (see hicache_load_burst); NULL = one launch per layer */
   int64_t burst_words_len; /* number of uint32 words at burst_words */
+  void* index_staging;     /* optional device memory for host-located indices: after validating
+                              them the call copies both arrays here (stream-ordered) and the kernels
+                              read them from HBM instead of across the host link; needs
+                              hicache_index_staging_bytes(n, index_bits) bytes, 16-byte aligned */
+  size_t index_staging_bytes; /* bytes at index_staging */
 } hicache_opts;
 
 /*
@@ -240,6 +245,10 @@ hicache_status hicache_backup_all_layers_static_staging(const hicache_pool* pool
                                                         int32_t index_bits, int64_t n,
                                                         const hicache_opts* opts,
                                                         cudaStream_t stream);
+
+/* Bytes of opts->index_staging that a call with n pairs of index_bits-bit
+ * indices needs (both arrays, each 16-byte aligned). */
+size_t hicache_index_staging_bytes(int64_t n, int32_t index_bits);
 
 /* One maximal run of pairs: device slots d0.., host slots h0.., len pairs. */
 typedef struct hicache_run {

@@ -47,14 +47,24 @@ BURSTS = ["per_layer", "single_launch"]
 
 # ---------------------------------------------------------------- tiny MHA pool
 
-@pytest.mark.parametrize("where", ["device", "host"])
+def _index_staging(n, dtype=torch.int64):
+    bits = 32 if dtype == torch.int32 else 64
+    return torch.empty(hk.index_staging_bytes(n, bits), dtype=torch.uint8, device="cuda")
+
+
+@pytest.mark.parametrize("where", ["device", "host", "host_staged_idx"])
 @pytest.mark.parametrize("dtype", [torch.int32, torch.int64])
 @pytest.mark.parametrize("path", ["zero_copy", "staged", "zero_copy_single_launch"])
 def test_tiny_mha_backup_then_load(where, dtype, path):
+    """host_staged_idx: host-located indices copied by the library into opts.index_staging."""
     wl = W.tiny_mha()
     s = wl.pools[0]
     if path == "staged" and where == "device":
         pytest.skip("the staged path plans DMA spans on the CPU: host-located indices only")
+    extra = {}
+    if where == "host_staged_idx":
+        where = "host"
+        extra["index_staging"] = _index_staging(wl.move_pages * s.page_size, dtype)
     pool = G.make_pool(s, seed=wl.seed)
     d, h, dp, hp = W.page_pairs(wl.seed, wl.move_pages, s.device_slots // s.page_size,
                                 s.host_pages, s.page_size)
@@ -63,11 +73,12 @@ def test_tiny_mha_backup_then_load(where, dtype, path):
     if path == "staged":
         # room for 5 host pages of all layers: 64 pages take 13 chunks, both buffers alternate
         per_page = s.num_tensors * s.num_layers * s.page_size * s.row_bytes
-        opts = _opts(hk.HICACHE_PATH_STAGED, where, staging=_staging(5 * per_page))
+        opts = _opts(hk.HICACHE_PATH_STAGED, where, staging=_staging(5 * per_page), **extra)
     elif path == "zero_copy_single_launch":
-        opts = _opts(hk.HICACHE_PATH_ZERO_COPY, where, burst_words=_burst_words(s.num_layers))
+        opts = _opts(hk.HICACHE_PATH_ZERO_COPY, where, burst_words=_burst_words(s.num_layers),
+                     **extra)
     else:
-        opts = _opts(hk.HICACHE_PATH_ZERO_COPY, where)
+        opts = _opts(hk.HICACHE_PATH_ZERO_COPY, where, **extra)
     hk.hicache_backup_all_layers(pool, dt, ht, opts=opts)
     torch.cuda.synchronize()
     G.oracle_backup(pool, dev0, host0, d, h)
@@ -231,7 +242,8 @@ def test_two_pools_mla_and_indexer(path):
         opts = _opts(hk.HICACHE_PATH_STAGED, "host", staging=_staging(2 * per_page + 4096))
     elif path == "zero_copy_single_launch":
         opts = _opts(hk.HICACHE_PATH_ZERO_COPY, "host",
-                     burst_words=_burst_words(lat_s.num_layers))
+                     burst_words=_burst_words(lat_s.num_layers),
+                     index_staging=_index_staging(d.size))
     else:
         opts = _opts(hk.HICACHE_PATH_ZERO_COPY, "host")
     hk.hicache_backup_all_layers(pools, dt, ht, opts=opts)
@@ -468,6 +480,27 @@ def test_failed_burst_still_records_every_event():
         hk.hicache_load_burst(pool, 1, 5, ht, dt, layer_done=events)
     assert ei.value.status == hk.HICACHE_ERANGE
     assert not any(e.query() for e in events), "events were not re-recorded behind the sleep"
+    torch.cuda.synchronize()
+    assert all(e.query() for e in events)
+    G.assert_device_equal(pool, dev0, "rejected burst moved bytes")
+
+
+def test_short_index_staging_rejected_and_events_recorded():
+    s = G.shape(L=3, T=1, head_num=1, head_dim=64, dtype_size=2, P=4, slots=256, pages=16)
+    pool = G.make_pool(s, 21)
+    dev0 = G.device_images(pool)
+    dt, ht = G.index_tensors(np.arange(8), np.arange(8) + 16, "host")
+    events = [torch.cuda.Event() for _ in range(3)]
+    for e in events:
+        e.record()
+    torch.cuda.synchronize()
+    torch.cuda._sleep(200_000_000)
+    small = torch.empty(hk.index_staging_bytes(8, 64) - 16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(hk.HiCacheError) as ei:
+        hk.hicache_load_burst(pool, 0, 3, ht, dt, layer_done=events,
+                              opts=_opts(hk.HICACHE_PATH_ZERO_COPY, "host", index_staging=small))
+    assert ei.value.status == hk.HICACHE_EINVAL and "index_staging" in ei.value.message
+    assert not any(e.query() for e in events)
     torch.cuda.synchronize()
     assert all(e.query() for e in events)
     G.assert_device_equal(pool, dev0, "rejected burst moved bytes")
