@@ -470,10 +470,11 @@ def run_ours(args, rank, world):
     res = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(total_ms / K, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "u8 (opaque bf16 KV bytes)",
+        "scaling": "weak", "vs_baseline": None, "dtype": "u8",
         "data": "synthetic (seeded bf16 ~N(0,1) pools, seeded random page lists)",
         "config": {
             "workload": wl.name, "description": wl.description,
+            "values": "bf16 ~N(0,1) KV bytes (uint8 for indexer / SSM state), moved opaquely",
             "pages_per_op": wl.move_pages, "tokens_per_op": int(n), "layers": L,
             "step": "all-layer D2H backup + H2D per-layer load-back burst with layer events",
             "step_payload_bytes": int(step_bytes), "path": args.path, "burst": args.burst,
