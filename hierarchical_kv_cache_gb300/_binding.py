@@ -10,7 +10,7 @@ from __future__ import annotations
 
 import ctypes
 import os
-from dataclasses import dataclass, field
+from dataclasses import dataclass
 from typing import Optional, Sequence
 
 import numpy as np
@@ -122,7 +122,6 @@ class Pool:
     host_pages: int
     page_granular: bool = False
     layout: int = HICACHE_LAYOUT_PAGE_FIRST_DIRECT
-    _keep: list = field(default_factory=list, repr=False)
 
     @property
     def num_tensors(self) -> int:
@@ -132,19 +131,24 @@ class Pool:
     def row_bytes(self) -> int:
         return self.head_num * self.head_dim * self.dtype_size
 
-    def to_c(self) -> c_pool:
+    def to_c(self):
+        """(c_pool, keep): the struct and the pointer arrays it points into.
+
+        The caller holds `keep` until the C call returns; nothing is stored on the
+        Pool, so threads may share one Pool.
+        """
         T, L = self.num_tensors, self.num_layers
         dev = (ctypes.c_void_p * (T * L))(*[self.device_layers[t][l].data_ptr()
                                             for t in range(T) for l in range(L)])
         host = (ctypes.c_void_p * T)(*[h.data_ptr() for h in self.host_tensors])
-        self._keep = [dev, host]
-        return c_pool(num_layers=L, num_tensors=T, head_num=self.head_num,
-                      head_dim=self.head_dim, dtype_size=self.dtype_size,
-                      page_size=self.page_size, page_granular=int(self.page_granular),
-                      layout=int(self.layout), device_slots=self.device_slots,
-                      host_pages=self.host_pages,
-                      device_layers=ctypes.cast(dev, ctypes.POINTER(ctypes.c_void_p)),
-                      host_tensors=ctypes.cast(host, ctypes.POINTER(ctypes.c_void_p)))
+        st = c_pool(num_layers=L, num_tensors=T, head_num=self.head_num,
+                    head_dim=self.head_dim, dtype_size=self.dtype_size,
+                    page_size=self.page_size, page_granular=int(self.page_granular),
+                    layout=int(self.layout), device_slots=self.device_slots,
+                    host_pages=self.host_pages,
+                    device_layers=ctypes.cast(dev, ctypes.POINTER(ctypes.c_void_p)),
+                    host_tensors=ctypes.cast(host, ctypes.POINTER(ctypes.c_void_p)))
+        return st, (dev, host)
 
 
 @dataclass
@@ -162,10 +166,12 @@ class Opts:
 
 
 def _pools_arg(pools):
+    """(array of c_pool, count, keep); keep must outlive the C call."""
     if not isinstance(pools, (list, tuple)):
         pools = [pools]
-    arr = (c_pool * len(pools))(*[p.to_c() for p in pools])
-    return arr, len(pools), pools
+    built = [p.to_c() for p in pools]
+    arr = (c_pool * len(pools))(*[b[0] for b in built])
+    return arr, len(pools), [b[1] for b in built]
 
 
 def _index_bits(t) -> int:
@@ -231,12 +237,13 @@ def _indices(a, b):
 def hicache_backup_all_layers(pools, device_indices, host_indices, *, opts: Optional[Opts] = None,
                               stream=None) -> None:
     """All-layer D2H backup of pairs device_indices[i] -> host_indices[i] (see hicache.h)."""
-    arr, npools, _ = _pools_arg(pools)
+    arr, npools, keep = _pools_arg(pools)
     bits, n = _indices(device_indices, host_indices)
     o = _opts_arg(opts, device_indices, host_indices)
     _check(lib().hicache_backup_all_layers(arr, npools, device_indices.data_ptr(),
                                            host_indices.data_ptr(), bits, n, ctypes.byref(o),
                                            _stream_arg(stream)))
+    del keep  # the pointer arrays lived until the call returned
 
 
 def hicache_backup_all_layers_static_staging(pools, device_indices, host_indices, *,
@@ -249,30 +256,32 @@ def hicache_backup_all_layers_static_staging(pools, device_indices, host_indices
     host tensors covering whole host pages; one host page of all layers must fit
     in 16 MiB.  Calls that overlap on the GPU share the static array and race.
     """
-    arr, npools, _ = _pools_arg(pools)
+    arr, npools, keep = _pools_arg(pools)
     bits, n = _indices(device_indices, host_indices)
     o = _opts_arg(opts, device_indices, host_indices)
     _check(lib().hicache_backup_all_layers_static_staging(
         arr, npools, device_indices.data_ptr(), host_indices.data_ptr(), bits, n,
         ctypes.byref(o), _stream_arg(stream)))
+    del keep  # the pointer arrays lived until the call returned
 
 
 def hicache_load_layer(pools, layer: int, host_indices, device_indices, *,
                        opts: Optional[Opts] = None, stream=None, layer_done=None) -> None:
     """H2D load-back of one layer; records ``layer_done`` (a torch.cuda.Event) after it."""
-    arr, npools, _ = _pools_arg(pools)
+    arr, npools, keep = _pools_arg(pools)
     bits, n = _indices(device_indices, host_indices)
     o = _opts_arg(opts, device_indices, host_indices)
     s = _stream_arg(stream)
     _check(lib().hicache_load_layer(arr, npools, layer, host_indices.data_ptr(),
                                     device_indices.data_ptr(), bits, n, ctypes.byref(o), s,
                                     _event_handle(layer_done, s)))
+    del keep  # the pointer arrays lived until the call returned
 
 
 def hicache_load_burst(pools, layer_begin: int, layer_end: int, host_indices, device_indices, *,
                        opts: Optional[Opts] = None, stream=None, layer_done=None) -> None:
     """H2D load-back of layers [layer_begin, layer_end), one event per layer (list or None)."""
-    arr, npools, _ = _pools_arg(pools)
+    arr, npools, keep = _pools_arg(pools)
     bits, n = _indices(device_indices, host_indices)
     o = _opts_arg(opts, device_indices, host_indices)
     s = _stream_arg(stream)
@@ -284,6 +293,7 @@ def hicache_load_burst(pools, layer_begin: int, layer_end: int, host_indices, de
         evs = (ctypes.c_void_p * max(1, count))(*[_event_handle(e, s) for e in layer_done])
     _check(lib().hicache_load_burst(arr, npools, layer_begin, layer_end, host_indices.data_ptr(),
                                     device_indices.data_ptr(), bits, n, ctypes.byref(o), s, evs))
+    del keep  # the pointer arrays lived until the call returned
 
 
 def hicache_plan_runs(device_indices, host_indices, page_size: int):
@@ -307,11 +317,12 @@ def hicache_plan_runs(device_indices, host_indices, page_size: int):
 def hicache_layer_checksum(pool: Pool, tensor: int, layer: int, device_indices, out_sum, *,
                            stream=None) -> None:
     """Adds the 32-bit words of the indexed rows into ``out_sum`` (a zeroed int64 CUDA tensor)."""
-    arr, _, _ = _pools_arg(pool)
+    arr, _, keep = _pools_arg(pool)
     bits = _index_bits(device_indices)
     _check(lib().hicache_layer_checksum(arr, tensor, layer, device_indices.data_ptr(), bits,
                                         device_indices.numel(), out_sum.data_ptr(),
                                         _stream_arg(stream)))
+    del keep  # the pointer arrays lived until the call returned
 
 
 def abi_version() -> int:
