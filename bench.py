@@ -353,6 +353,7 @@ def run_ours(args, rank, world):
 
     path = {"auto": hk.HICACHE_PATH_AUTO, "zero_copy": hk.HICACHE_PATH_ZERO_COPY,
             "staged": hk.HICACHE_PATH_STAGED}[args.path]
+    staged = args.path == "staged"
     staging = None
     if args.path != "zero_copy":
         staging = [torch.empty(args.staging_mib << 20, dtype=torch.uint8, device="cuda")
@@ -508,9 +509,13 @@ def run_ours(args, rank, world):
         "roofline_backup": {
             "bound": "host_link", "achieved": round(backup_gbs, 2), "peak": round(link["d2h"], 2),
             "unit": "GB/s", "frac": round(backup_gbs / link["d2h"], 4),
-            "traffic": traffic_per_launch("backup_all_layers", bytes_backup),
-            "kernel": "row_copy_kernel<int64,512,static>: one all-layer backup launch "
-                      f"({bytes_backup} algorithmic bytes = n x L x T x R)",
+            "traffic": (None if staged else
+                        traffic_per_launch("backup_all_layers", bytes_backup)),
+            "kernel": ("staged backup: gather kernels into two HBM staging buffers, then one "
+                       "cudaMemcpyAsync per host-page run, whole operation"
+                       if staged else
+                       "row_copy_kernel<int64,512,static>: one all-layer backup launch")
+                      + f" ({bytes_backup} algorithmic bytes = n x L x T x R)",
             "peak_source": "pinned cudaMemcpyAsync D2H measured in this run (of measured); "
                            "HBM is not the bound: the launch reads its payload once from HBM",
             "hbm_frac_of_measured": round(backup_gbs / hbm_peak(), 4),
@@ -520,13 +525,18 @@ def run_ours(args, rank, world):
             "bound": "host_link", "achieved": round(layer_gbs, 2) if layer_gbs else None,
             "peak": round(link["h2d"], 2), "unit": "GB/s",
             "frac": round(layer_gbs / link["h2d"], 4) if layer_gbs else None,
-            "traffic": traffic_per_launch("load_one_layer" if args.burst == "per_layer"
-                                          else "load_burst_signalling", bytes_layer),
-            "kernel": ("row_copy_kernel<int64,16,8>: one per-layer load launch"
+            "traffic": (None if staged else
+                        traffic_per_launch("load_one_layer" if args.burst == "per_layer"
+                                           else "load_burst_signalling", bytes_layer)),
+            "kernel": ("staged load of one layer: cudaMemcpy2DAsync per host-page run into "
+                       "HBM staging, then a scatter kernel (event-to-event)"
+                       if staged else
+                       "row_copy_kernel<int64,16,8>: one per-layer load launch"
                        if args.burst == "per_layer" else
                        "row_copy_kernel<int64,16,512,signalling>: one layer of the "
                        "single-launch burst (event-to-event)")
                       + f" ({bytes_layer} algorithmic bytes = n x T x R), median of the burst",
+            "ms_per_launch": round(bytes_layer / (layer_gbs * GB) * 1e3, 4) if layer_gbs else None,
         },
         "roofline_step": {
             "bound": "host_link", "achieved": round(achieved, 2), "peak": round(peak_mix, 2),
@@ -555,6 +565,8 @@ def run_ours(args, rank, world):
             "ms_per_launch": round(mr, 4),
         }
         dominant = "roofline_burst" if mr > mb else "roofline_backup"
+    elif staged and ml > mb and layer_gbs:
+        dominant = "roofline_load"  # the staged load-back takes most of the step
     else:
         dominant = "roofline_backup"
     res["roofline"] = dict(res[dominant], which=dominant)
