@@ -70,6 +70,8 @@ def parse_args():
     ap.add_argument("--sweep-rows", default="16,64,256,1152,2048")
     ap.add_argument("--sweep-pages", default="1,16,64,256")
     ap.add_argument("--sweep-tokens", default="1024,4096,16384,65536,262144")
+    ap.add_argument("--dma-sweep", action="store_true",
+                    help="measure the copy engine's cost per copy against the copy size instead")
     return ap.parse_args()
 
 
@@ -445,6 +447,8 @@ def run_ours(args, rank, world):
     backup_gbs = bytes_backup / (mb * 1e-3) / GB
     load_gbs = bytes_load / (ml * 1e-3) / GB
     layer_gbs = bytes_layer / (statistics.median(per_layer) * 1e-3) / GB if per_layer else None
+    if staged:
+        layer_gbs = None  # the staged load lands layers in groups: only the burst has a rate
     first_us = statistics.mean(t_first) * 1e3
     bound_us = ml * 1e3 / L + 20.0
     # time-weighted link peak of the step's mix of directions
@@ -521,23 +525,26 @@ def run_ours(args, rank, world):
             "hbm_frac_of_measured": round(backup_gbs / hbm_peak(), 4),
             "ms_per_launch": round(mb, 4),
         },
-        "roofline_load": {
+        "roofline_load": ({
+            "bound": "host_link", "achieved": round(load_gbs, 2), "peak": round(link["h2d"], 2),
+            "unit": "GB/s", "frac": round(load_gbs / link["h2d"], 4), "traffic": None,
+            "kernel": "staged load burst: one cudaMemcpy2DAsync per host-page run and layer "
+                      "group into HBM staging, then one scatter launch per layer, whole burst "
+                      f"({bytes_load} algorithmic bytes = n x L x T x R)",
+            "ms_per_launch": round(ml, 4),
+        } if staged else {
             "bound": "host_link", "achieved": round(layer_gbs, 2) if layer_gbs else None,
             "peak": round(link["h2d"], 2), "unit": "GB/s",
             "frac": round(layer_gbs / link["h2d"], 4) if layer_gbs else None,
-            "traffic": (None if staged else
-                        traffic_per_launch("load_one_layer" if args.burst == "per_layer"
-                                           else "load_burst_signalling", bytes_layer)),
-            "kernel": ("staged load of one layer: cudaMemcpy2DAsync per host-page run into "
-                       "HBM staging, then a scatter kernel (event-to-event)"
-                       if staged else
-                       "row_copy_kernel<int64,16,8>: one per-layer load launch"
+            "traffic": traffic_per_launch("load_one_layer" if args.burst == "per_layer"
+                                          else "load_burst_signalling", bytes_layer),
+            "kernel": ("row_copy_kernel<int64,16,8>: one per-layer load launch"
                        if args.burst == "per_layer" else
                        "row_copy_kernel<int64,16,512,signalling>: one layer of the "
                        "single-launch burst (event-to-event)")
                       + f" ({bytes_layer} algorithmic bytes = n x T x R), median of the burst",
             "ms_per_launch": round(bytes_layer / (layer_gbs * GB) * 1e3, 4) if layer_gbs else None,
-        },
+        }),
         "roofline_step": {
             "bound": "host_link", "achieved": round(achieved, 2), "peak": round(peak_mix, 2),
             "unit": "GB/s", "frac": round(achieved / peak_mix, 4),
@@ -565,7 +572,7 @@ def run_ours(args, rank, world):
             "ms_per_launch": round(mr, 4),
         }
         dominant = "roofline_burst" if mr > mb else "roofline_backup"
-    elif staged and ml > mb and layer_gbs:
+    elif staged and ml > mb:
         dominant = "roofline_load"  # the staged load-back takes most of the step
     else:
         dominant = "roofline_backup"
@@ -917,10 +924,78 @@ def run_sweep(args):
     print(json.dumps({"sweep_points": len(out), "link_peak_gbs": link}), flush=True)
 
 
+def run_dma_sweep(args):
+    """The copy engine's cost per copy, against the copy size.
+
+    Copies of one size between random 4 MiB pages of a pinned host buffer and
+    HBM, issued on 1 or 4 streams behind a sleep kernel, so that the timed
+    region holds the copies only and not the host's enqueue.  This is what
+    bounds the staged path: it issues one copy per host-page run (and layer
+    group), and on GB300 a copy costs a few microseconds whatever its size.
+    """
+    import numpy as np
+    import torch
+    torch.cuda.set_device(0)
+    page, pages = 4 << 20, 1024
+    host = torch.empty(pages * page, dtype=torch.uint8, pin_memory=True)  # 4 GiB
+    host.fill_(1)
+    dev = torch.empty(64 << 20, dtype=torch.uint8, device="cuda")
+    pick = np.random.default_rng(1).permutation(pages)[:256]
+    streams = [torch.cuda.Stream() for _ in range(4)]
+    main_s = torch.cuda.Stream()
+    out = []
+    for direction in ("h2d", "d2h"):
+        for block in (128 << 10, 256 << 10, 512 << 10, 1 << 20, 2 << 20, 4 << 20):
+            ncopy = min(256, (64 << 20) // block)
+            for nstreams in (1, 4):
+                times, enq = [], []
+                for rep in range(6):
+                    torch.cuda.synchronize()
+                    t0 = torch.cuda.Event(enable_timing=True)
+                    t1 = torch.cuda.Event(enable_timing=True)
+                    with torch.cuda.stream(main_s):
+                        torch.cuda._sleep(100_000_000)  # ~50 ms: the copies queue up behind it
+                        t0.record(main_s)
+                    for st in streams[:nstreams]:
+                        st.wait_stream(main_s)
+                    w0 = time.perf_counter()
+                    for k in range(ncopy):
+                        st = streams[k % nstreams]
+                        h = host[int(pick[k]) * page:int(pick[k]) * page + block]
+                        d = dev[k * block:(k + 1) * block]
+                        with torch.cuda.stream(st):
+                            if direction == "h2d":
+                                d.copy_(h, non_blocking=True)
+                            else:
+                                h.copy_(d, non_blocking=True)
+                    enq.append(time.perf_counter() - w0)
+                    for st in streams[:nstreams]:
+                        main_s.wait_stream(st)
+                    t1.record(main_s)
+                    t1.synchronize()
+                    if rep:
+                        times.append(t0.elapsed_time(t1))
+                ms = statistics.median(times)
+                rec = {"direction": direction, "copy_bytes": block, "copies": ncopy,
+                       "streams": nstreams, "ms": round(ms, 4),
+                       "us_per_copy": round(ms * 1e3 / ncopy, 2),
+                       "gbs": round(ncopy * block / (ms * 1e-3) / GB, 2),
+                       "enqueue_hidden": max(enq) < 0.04}
+                out.append(rec)
+                print(json.dumps(rec), flush=True)
+    if args.out:
+        with open(args.out, "w") as f:
+            for rec in out:
+                f.write(json.dumps(rec) + "\n")
+
+
 def main():
     args = parse_args()
     if args.sweep:
         run_sweep(args)
+        return
+    if args.dma_sweep:
+        run_dma_sweep(args)
         return
     if args.impl == "reference":
         rank = int(os.environ.get("RANK", "0"))

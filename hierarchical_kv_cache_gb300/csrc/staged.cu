@@ -12,6 +12,7 @@
 // indices on the host, because the DMA spans are planned on the CPU.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <string>
 #include <vector>
 
@@ -57,23 +58,22 @@ hicache_status get_res(StagedRes** out) {
 }
 
 // Staging layout: one region per (pool, tensor), each `cap_pages` pages of
-// `page_bytes(pool)` bytes; region offsets are in (pool, tensor) order.
+// `layers` layer blocks; region offsets are in (pool, tensor) order.
 struct StagingLayout {
   int64_t cap_pages = 0;
   std::vector<std::vector<int64_t>> region_off;  // [pool][tensor]
 };
 
 StagingLayout layout_for(const std::vector<PoolInfo>& pools, const hicache_opts& o,
-                         bool all_layers) {
+                         int32_t layers) {
   StagingLayout s;
   int64_t per_page = 0;
-  for (const PoolInfo& pi : pools)
-    per_page += int64_t(pi.T) * (all_layers ? pi.L : 1) * pi.P * pi.token_bytes;
+  for (const PoolInfo& pi : pools) per_page += int64_t(pi.T) * layers * pi.P * pi.token_bytes;
   s.cap_pages = per_page > 0 ? int64_t(o.staging_bytes) / per_page : 0;
   int64_t off = 0;
   for (const PoolInfo& pi : pools) {
     std::vector<int64_t> offs;
-    const int64_t region = s.cap_pages * (all_layers ? pi.L : 1) * pi.P * pi.token_bytes;
+    const int64_t region = s.cap_pages * layers * pi.P * pi.token_bytes;
     for (int32_t t = 0; t < pi.T; ++t) {
       offs.push_back(off);
       off += region;
@@ -83,8 +83,12 @@ StagingLayout layout_for(const std::vector<PoolInfo>& pools, const hicache_opts&
   return s;
 }
 
+// A staging buffer as a paged side holding `layers` consecutive layers of each
+// page, starting at layer `layer_origin`, laid out like a host page of that
+// many layers: [page][layer][token][row] for page_first_direct pools,
+// [token][layer][row] for page_first pools.
 SideSpec staging_side(const std::vector<PoolInfo>& pools, const StagingLayout& lay, char* base,
-                      bool all_layers, int32_t layer_origin) {
+                      int32_t layers, int32_t layer_origin) {
   SideSpec side;
   side.layer_origin = layer_origin;
   for (size_t p = 0; p < pools.size(); ++p) {
@@ -92,17 +96,14 @@ SideSpec staging_side(const std::vector<PoolInfo>& pools, const StagingLayout& l
     std::vector<char*> b;
     for (int32_t t = 0; t < pi.T; ++t) b.push_back(base + lay.region_off[p][size_t(t)]);
     const int64_t block = int64_t(pi.P) * pi.token_bytes;  // one (page, layer) block
-    const bool direct = pi.layout == HICACHE_LAYOUT_PAGE_FIRST_DIRECT;
-    if (all_layers && !direct) {
-      // backup staging mirrors a token-major host page: [token][layer][row]
-      side.layer_stride.push_back(pi.token_bytes);
-      side.page_stride.push_back(int64_t(pi.L) * pi.token_bytes);
-      side.rows_per_page.push_back(1);
-    } else {
-      // [page][layer][token][row] (backup), or one layer: [page][token][row] (load)
-      side.layer_stride.push_back(all_layers ? block : 0);
-      side.page_stride.push_back(all_layers ? block * pi.L : block);
+    if (pi.layout == HICACHE_LAYOUT_PAGE_FIRST_DIRECT) {
+      side.layer_stride.push_back(block);
+      side.page_stride.push_back(block * layers);
       side.rows_per_page.push_back(moves_page_rows(pi) ? 1 : pi.P);
+    } else {
+      side.layer_stride.push_back(pi.token_bytes);
+      side.page_stride.push_back(int64_t(layers) * pi.token_bytes);
+      side.rows_per_page.push_back(1);
     }
     side.paged_tokens.push_back(lay.cap_pages * pi.P);
     side.vec16.push_back(vec16_ok(pi, b, side.layer_stride.back()));
@@ -151,7 +152,7 @@ hicache_status staged_backup(const std::vector<PoolInfo>& pools, const hicache_o
   std::vector<int64_t> hp;
   hicache_status st = need_pages(idx, P, &hp);
   if (st != HICACHE_OK) return st;
-  const StagingLayout lay = layout_for(pools, o, /*all_layers=*/true);
+  const StagingLayout lay = layout_for(pools, o, L);
   if (lay.cap_pages < 1)
     return fail(HICACHE_ENOSTAGE, "staging buffers hold less than one host page of all layers");
   StagedRes* r = nullptr;
@@ -160,8 +161,8 @@ hicache_status staged_backup(const std::vector<PoolInfo>& pools, const hicache_o
   cudaStream_t copy = o.copy_stream ? o.copy_stream : r->copy;
   const LaunchCfg cfg{o.max_ctas, o.device_error, /*paged_in_hbm=*/true};
   const int64_t groups = int64_t(hp.size());
-  const SideSpec side[2] = {staging_side(pools, lay, static_cast<char*>(o.staging[0]), true, 0),
-                            staging_side(pools, lay, static_cast<char*>(o.staging[1]), true, 0)};
+  const SideSpec side[2] = {staging_side(pools, lay, static_cast<char*>(o.staging[0]), L, 0),
+                            staging_side(pools, lay, static_cast<char*>(o.staging[1]), L, 0)};
 
   HK_CUDA(cudaEventRecord(r->fork, stream), "cudaEventRecord(fork)");
   HK_CUDA(cudaStreamWaitEvent(copy, r->fork, 0), "cudaStreamWaitEvent(fork)");
@@ -197,46 +198,72 @@ hicache_status staged_backup(const std::vector<PoolInfo>& pools, const hicache_o
   return HICACHE_OK;
 }
 
+// The copy engine costs about 4 microseconds per copy on GB300, whatever the
+// number of streams or host threads issuing them: a 128 KiB copy (one layer of
+// one 64-token page of 2 KiB rows) moves 33 GB/s, a 512 KiB copy 106 GB/s,
+// 2 MiB 170 GB/s and 4 MiB 186 GB/s (host to device).  The staged load
+// therefore copies a group of consecutive layers of each host page per DMA
+// (they are adjacent in a page-first host page) and lets the groups grow
+// 1, 2, 4, ... layers until one copy carries about this many bytes, so that
+// the first layer still lands after one layer's transfer.
+constexpr int64_t kDmaCopyTargetBytes = int64_t(4) << 20;
+// A group too large for the staging to hold every page at once moves in
+// chunks of pages; a chunk holds at least this many pages (or all of them),
+// so that the per-chunk scatter launch and stream hand-offs stay small next
+// to its copies.
+constexpr int64_t kMinChunkPages = 32;
+
 hicache_status staged_load(const std::vector<PoolInfo>& pools, const hicache_opts& o,
                            const IndexSet& idx, int32_t layer_begin, int32_t layer_end,
                            cudaStream_t stream, cudaEvent_t* layer_done) {
   const int32_t P = pools[0].P;
   const int32_t L = pools[0].L;
   const int32_t count = layer_end - layer_begin;
-  auto finish = [&](int32_t from, hicache_status s) {
+  int32_t recorded = 0;  // layer events recorded so far, in order
+  auto finish = [&](hicache_status s) {
     // a failed load still completes every remaining layer event
-    for (int32_t i = from; i < count; ++i)
+    for (int32_t i = recorded; i < count; ++i)
       if (layer_done && layer_done[i]) cudaEventRecord(layer_done[i], stream);
     return s;
   };
   std::vector<int64_t> hp;
   hicache_status st = need_pages(idx, P, &hp);
-  if (st != HICACHE_OK) return finish(0, st);
-  const StagingLayout lay = layout_for(pools, o, /*all_layers=*/false);
-  if (lay.cap_pages < 1)
-    return finish(0, fail(HICACHE_ENOSTAGE, "staging buffers hold less than one host page of one layer"));
+  if (st != HICACHE_OK) return finish(st);
+  if (layout_for(pools, o, 1).cap_pages < 1)
+    return finish(fail(HICACHE_ENOSTAGE, "staging buffers hold less than one host page of one layer"));
   StagedRes* r = nullptr;
   st = get_res(&r);
-  if (st != HICACHE_OK) return finish(0, st);
+  if (st != HICACHE_OK) return finish(st);
   cudaStream_t copy = o.copy_stream ? o.copy_stream : r->copy;
   const LaunchCfg cfg{o.max_ctas, o.device_error, /*paged_in_hbm=*/true};
   const int64_t groups = int64_t(hp.size());
+  int64_t max_block = 1;
+  for (const PoolInfo& pi : pools) max_block = std::max(max_block, int64_t(pi.P) * pi.token_bytes);
+  const int32_t g_cap = int32_t(std::min<int64_t>(
+      count, std::max<int64_t>(1, (kDmaCopyTargetBytes + max_block - 1) / max_block)));
 
 #define HK_TRY(call, what)                                    \
   do {                                                        \
     const cudaError_t e_ = (call);                            \
-    if (e_ != cudaSuccess) return finish(l - layer_begin, cuda_fail(e_, what)); \
+    if (e_ != cudaSuccess) return finish(cuda_fail(e_, what)); \
   } while (0)
 
-  int32_t l = layer_begin;
   HK_TRY(cudaEventRecord(r->fork, stream), "cudaEventRecord(fork)");
   HK_TRY(cudaStreamWaitEvent(copy, r->fork, 0), "cudaStreamWaitEvent(fork)");
   int64_t step = 0;
-  for (; l < layer_end; ++l) {
+  int32_t g_want = 1;
+  for (int32_t l = layer_begin, g = 1; l < layer_end; l += g) {
+    // the largest group (up to g_want) whose chunks hold kMinChunkPages
+    // pages, or every page; one layer per group when not even that fits
+    g = std::min(g_want, layer_end - l);
+    while (g > 1 && layout_for(pools, o, g).cap_pages < std::min(groups, kMinChunkPages)) --g;
+    g_want = std::min(g_cap, 2 * g_want);
+    const StagingLayout lay = layout_for(pools, o, g);
     for (int64_t g0 = 0; g0 < groups; g0 += lay.cap_pages, ++step) {
       const int b = int(step & 1);
       const int64_t g1 = std::min(groups, g0 + lay.cap_pages);
-      const SideSpec side = staging_side(pools, lay, static_cast<char*>(o.staging[b]), false, l);
+      const bool last_chunk = g1 == groups;
+      const SideSpec side = staging_side(pools, lay, static_cast<char*>(o.staging[b]), g, l);
       // the scatter of step-2 must have read buffer b before the DMA refills it
       if (step >= 2) HK_TRY(cudaStreamWaitEvent(copy, r->freed[b], 0), "cudaStreamWaitEvent(freed)");
       for (size_t p = 0; p < pools.size(); ++p) {
@@ -249,16 +276,17 @@ hicache_status staged_load(const std::vector<PoolInfo>& pools, const hicache_opt
           for (int64_t j = g0; j < g1;) {
             int64_t e = j + 1;
             while (e < g1 && hp[size_t(e)] == hp[size_t(e - 1)] + 1) ++e;
-            char* dst = side.base[p][size_t(t)] + (j - g0) * block;
+            char* dst = side.base[p][size_t(t)] + (j - g0) * block * g;
             const char* page0 = pi.host[size_t(t)] + hp[size_t(j)] * host_page;
-            // direct: one contiguous block per page, pages host_page apart;
-            // page_first: one row per token, tokens L * R apart
+            // direct: layers l..l+g-1 of a page are one contiguous span, pages
+            // host_page apart; page_first: they are contiguous per token, tokens
+            // L * R apart
             const cudaError_t ce =
-                direct ? cudaMemcpy2DAsync(dst, size_t(block), page0 + int64_t(l) * block,
-                                           size_t(host_page), size_t(block), size_t(e - j),
+                direct ? cudaMemcpy2DAsync(dst, size_t(block * g), page0 + int64_t(l) * block,
+                                           size_t(host_page), size_t(block * g), size_t(e - j),
                                            cudaMemcpyHostToDevice, copy)
-                       : cudaMemcpy2DAsync(dst, size_t(R), page0 + int64_t(l) * R,
-                                           size_t(L) * size_t(R), size_t(R),
+                       : cudaMemcpy2DAsync(dst, size_t(R * g), page0 + int64_t(l) * R,
+                                           size_t(L) * size_t(R), size_t(R * g),
                                            size_t((e - j) * pi.P), cudaMemcpyHostToDevice, copy);
             HK_TRY(ce, "cudaMemcpy2DAsync(host -> staging)");
             j = e;
@@ -267,13 +295,23 @@ hicache_status staged_load(const std::vector<PoolInfo>& pools, const hicache_opt
       }
       HK_TRY(cudaEventRecord(r->ready[b], copy), "cudaEventRecord(ready)");
       HK_TRY(cudaStreamWaitEvent(stream, r->ready[b], 0), "cudaStreamWaitEvent(ready)");
-      st = launch_rows(pools, side, idx.dev_gpu, nullptr, idx.bits, g0 * P, (g1 - g0) * P,
-                       kPagedToDev, l, l + 1, cfg, stream);
-      if (st != HICACHE_OK) return finish(l - layer_begin, st);
+      if (!last_chunk) {
+        st = launch_rows(pools, side, idx.dev_gpu, nullptr, idx.bits, g0 * P, (g1 - g0) * P,
+                         kPagedToDev, l, l + g, cfg, stream);
+        if (st != HICACHE_OK) return finish(st);
+      } else {
+        // the group's last chunk: scatter layer by layer, each followed by its event
+        for (int32_t k = l; k < l + g; ++k) {
+          st = launch_rows(pools, side, idx.dev_gpu, nullptr, idx.bits, g0 * P, (g1 - g0) * P,
+                           kPagedToDev, k, k + 1, cfg, stream);
+          if (st != HICACHE_OK) return finish(st);
+          if (layer_done && layer_done[k - layer_begin])
+            HK_TRY(cudaEventRecord(layer_done[k - layer_begin], stream), "cudaEventRecord(layer_done)");
+          ++recorded;
+        }
+      }
       HK_TRY(cudaEventRecord(r->freed[b], stream), "cudaEventRecord(freed)");
     }
-    if (layer_done && layer_done[l - layer_begin])
-      HK_TRY(cudaEventRecord(layer_done[l - layer_begin], stream), "cudaEventRecord(layer_done)");
   }
 #undef HK_TRY
   return HICACHE_OK;

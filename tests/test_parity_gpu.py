@@ -317,7 +317,54 @@ def test_page_first_layout_backup_then_load(where, path):
     G.assert_device_equal(pool, dev1, "page_first burst")
 
 
-@pytest.mark.parametrize("path", ["zero_copy", "zero_copy_single_launch", "staged"])
+# (layout, moved pages, staging in layer blocks of every moved page, layer range).
+# Group sizes grow 1, 2, 4, ... while a staging buffer holds every page of the
+# group, or chunks of at least 32 pages of it.
+STAGED_GROUP_CASES = [
+    ("page_first_direct", 24, None, (0, 13)),   # groups 1, 2, 4, 6, one chunk each
+    ("page_first_direct", 24, 3, (0, 13)),      # groups 1, 2, 3, 3, 3, 1
+    ("page_first_direct", 24, None, (2, 11)),   # groups 1, 2, 4, 2 from layer 2
+    ("page_first", 24, None, (0, 13)),
+    ("page_first", 24, 3, (1, 12)),
+    # 80 pages, room for 40 pages of 4 layers: groups 1, 2, 4, 5, 1; the group of
+    # 4 moves in chunks of 40 + 40 pages, the group of 5 in 32 + 32 + 16
+    ("page_first_direct", 80, 2, (0, 13)),
+    ("page_first", 80, 2, (0, 13)),
+]
+
+
+@pytest.mark.parametrize("case", STAGED_GROUP_CASES,
+                         ids=[f"{c[0]}-n{c[1]}-stage{c[2]}-L{c[3][0]}_{c[3][1]}"
+                              for c in STAGED_GROUP_CASES])
+def test_staged_load_layer_groups(case):
+    """The staged load copies groups of consecutive layers per host page in one DMA."""
+    layout, npages, stage_layers, (l0, l1) = case
+    s = G.shape(L=13, T=2, head_num=2, head_dim=64, dtype_size=2, P=16, slots=4096, pages=128,
+                layout=layout)
+    pool = G.make_pool(s, seed=31)
+    P = s.page_size
+    d, h, dp, _ = W.page_pairs(32, npages, s.device_slots // P, s.host_pages, P)
+    dt, ht = G.index_tensors(d, h, "host")
+    per_layer = s.num_tensors * npages * P * s.row_bytes  # one layer of every moved page
+    layers = stage_layers if stage_layers is not None else s.num_layers
+    opts = _opts(hk.HICACHE_PATH_STAGED, "host", staging=_staging(layers * per_layer + 1000))
+    hk.hicache_backup_all_layers(pool, dt, ht, opts=opts)
+    torch.cuda.synchronize()
+    host0 = G.host_images(pool)
+    d2, _, _, _ = W.page_pairs(33, npages, s.device_slots // P, s.host_pages, P,
+                               exclude_device_pages=dp)
+    d2t, _ = G.index_tensors(d2, h, "host")
+    dev1 = G.device_images(pool)
+    events = [torch.cuda.Event() for _ in range(l1 - l0)]
+    hk.hicache_load_burst(pool, l0, l1, ht, d2t, opts=opts, layer_done=events)
+    torch.cuda.synchronize()
+    assert all(e.query() for e in events)
+    G.oracle_load(pool, dev1, host0, range(l0, l1), h, d2)
+    G.assert_device_equal(pool, dev1, f"staged layer groups {case}")
+
+
+@pytest.mark.parametrize("path", ["zero_copy", "zero_copy_single_launch", "staged",
+                                  "staged_groups"])
 def test_mixed_layouts_latent_direct_indexer_token_major(path):
     """Latent pool page_first_direct (16-byte chunks) with an indexer pool in the token-major
     layout (132-byte token rows, 4-byte chunks) in the same calls."""
@@ -331,9 +378,11 @@ def test_mixed_layouts_latent_direct_indexer_token_major(path):
     d, h, dp, _ = W.page_pairs(29, 7, 32, 20, P)
     imgs = [(G.device_images(p), G.host_images(p)) for p in pools]
     dt, ht = G.index_tensors(d, h, "host")
-    if path == "staged":
+    if path.startswith("staged"):
         per_page = sum(p.num_layers * P * p.row_bytes for p in pools)
-        opts = _opts(hk.HICACHE_PATH_STAGED, "host", staging=_staging(3 * per_page))
+        # 3 pages of all layers: one-layer loads; 7 pages: every layer of every page
+        opts = _opts(hk.HICACHE_PATH_STAGED, "host",
+                     staging=_staging((3 if path == "staged" else 7) * per_page))
     elif path == "zero_copy_single_launch":
         opts = _opts(hk.HICACHE_PATH_ZERO_COPY, "host", burst_words=_burst_words(4))
     else:
