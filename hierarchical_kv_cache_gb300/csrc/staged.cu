@@ -237,6 +237,7 @@ hicache_status staged_load(const std::vector<PoolInfo>& pools, const hicache_opt
   cudaStream_t copy = o.copy_stream ? o.copy_stream : r->copy;
   const LaunchCfg cfg{o.max_ctas, o.device_error, /*paged_in_hbm=*/true};
   const int64_t groups = int64_t(hp.size());
+  if (groups == 0) return finish(HICACHE_OK);  // nothing to move; the events still fire
   int64_t max_block = 1;
   for (const PoolInfo& pi : pools) max_block = std::max(max_block, int64_t(pi.P) * pi.token_bytes);
   const int32_t g_cap = int32_t(std::min<int64_t>(

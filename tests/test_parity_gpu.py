@@ -45,6 +45,26 @@ def _burst_words(layers):
 BURSTS = ["per_layer", "single_launch"]
 
 
+def _arm(events):
+    """Record the events once, then keep the current stream busy for ~0.1 s.
+
+    An event that was never recorded also reports complete, so a test that only
+    queries events cannot tell whether a call recorded them.  After _arm, an
+    event that a call records on the current stream stays incomplete until the
+    sleep ends, and one the call skipped reads complete at once.
+    """
+    for e in events:
+        e.record()
+    torch.cuda.synchronize()
+    torch.cuda._sleep(200_000_000)
+
+
+def _assert_recorded_behind_sleep(events):
+    assert not any(e.query() for e in events), "a layer event was not recorded by the call"
+    torch.cuda.synchronize()
+    assert all(e.query() for e in events)
+
+
 # ---------------------------------------------------------------- tiny MHA pool
 
 def _index_staging(n, dtype=torch.int64):
@@ -583,11 +603,11 @@ def test_single_launch_burst_with_no_rows_completes_events():
     dev0 = G.device_images(pool)
     dt, ht = G.index_tensors(np.arange(10), np.arange(10), "device")
     events = [torch.cuda.Event() for _ in range(3)]
+    _arm(events)
     hk.hicache_load_burst(pool, 0, 3, ht, dt, layer_done=events,
                           opts=_opts(hk.HICACHE_PATH_ZERO_COPY, "device",
                                      burst_words=_burst_words(3)))
-    torch.cuda.synchronize()
-    assert all(e.query() for e in events)
+    _assert_recorded_behind_sleep(events)
     G.assert_device_equal(pool, dev0, "no rows")
 
 
@@ -617,6 +637,49 @@ def test_staged_needs_staging_and_whole_pages():
     assert ei.value.status == hk.HICACHE_EINVAL
 
 
+@pytest.mark.parametrize("fault", ["no_staging", "small_staging", "partial_page"])
+def test_failed_staged_burst_still_records_every_event(fault):
+    s = G.shape(L=5, T=2, head_num=2, head_dim=64, dtype_size=2, P=16, slots=1024, pages=64)
+    pool = G.make_pool(s, 34)
+    dev0 = G.device_images(pool)
+    P = s.page_size
+    d, h, _, _ = W.page_pairs(35, 6, s.device_slots // P, s.host_pages, P)
+    if fault == "partial_page":
+        d, h = d[:-3], h[:-3]  # the last host page is not whole
+    dt, ht = G.index_tensors(d, h, "host")
+    staging = {"no_staging": None, "small_staging": _staging(P * s.row_bytes - 16),
+               "partial_page": _staging(1 << 20)}[fault]
+    events = [torch.cuda.Event() for _ in range(4)]
+    _arm(events)
+    with pytest.raises(hk.HiCacheError) as ei:
+        hk.hicache_load_burst(pool, 1, 5, ht, dt, layer_done=events,
+                              opts=_opts(hk.HICACHE_PATH_STAGED, "host", staging=staging))
+    assert ei.value.status == (hk.HICACHE_EINVAL if fault == "partial_page"
+                               else hk.HICACHE_ENOSTAGE)
+    _assert_recorded_behind_sleep(events)
+    G.assert_device_equal(pool, dev0, "rejected staged burst moved bytes")
+
+
+def test_staged_burst_records_every_event_in_groups():
+    """Layer groups record one event per layer, each after its own layer's scatter."""
+    s = G.shape(L=11, T=2, head_num=2, head_dim=64, dtype_size=2, P=16, slots=2048, pages=64)
+    pool = G.make_pool(s, 36)
+    P = s.page_size
+    d, h, _, _ = W.page_pairs(37, 20, s.device_slots // P, s.host_pages, P)
+    dt, ht = G.index_tensors(d, h, "host")
+    opts = _opts(hk.HICACHE_PATH_STAGED, "host",
+                 staging=_staging(s.num_layers * 20 * P * s.row_bytes * s.num_tensors))
+    hk.hicache_backup_all_layers(pool, dt, ht, opts=opts)
+    torch.cuda.synchronize()
+    host0, dev1 = G.host_images(pool), G.device_images(pool)
+    events = [torch.cuda.Event() for _ in range(s.num_layers)]
+    _arm(events)
+    hk.hicache_load_burst(pool, 0, s.num_layers, ht, dt, layer_done=events, opts=opts)
+    _assert_recorded_behind_sleep(events)
+    G.oracle_load(pool, dev1, host0, range(s.num_layers), h, d)
+    G.assert_device_equal(pool, dev1, "staged groups")
+
+
 def test_empty_lists_record_events_and_move_nothing():
     s = G.shape(L=3, T=2, head_num=2, head_dim=64, dtype_size=2, P=16, slots=1024, pages=64)
     pool = G.make_pool(s, 19)
@@ -624,18 +687,29 @@ def test_empty_lists_record_events_and_move_nothing():
     dt, ht = G.index_tensors(np.zeros(0, np.int64), np.zeros(0, np.int64), "device")
     events = [torch.cuda.Event() for _ in range(3)]
     hk.hicache_backup_all_layers(pool, dt, ht)
+    _arm(events)
     hk.hicache_load_burst(pool, 0, 3, ht, dt, layer_done=events)
-    torch.cuda.synchronize()
-    assert all(e.query() for e in events)
+    _assert_recorded_behind_sleep(events)
+    for opts in (_opts(hk.HICACHE_PATH_ZERO_COPY, "device", burst_words=_burst_words(3)),
+                 _opts(hk.HICACHE_PATH_STAGED, "host", staging=_staging(1 << 20))):
+        loc = "host" if opts.index_location == hk.HICACHE_INDEX_HOST else "device"
+        de, he = G.index_tensors(np.zeros(0, np.int64), np.zeros(0, np.int64), loc)
+        _arm(events)
+        hk.hicache_load_burst(pool, 0, 3, he, de, layer_done=events, opts=opts)
+        _assert_recorded_behind_sleep(events)
     G.assert_device_equal(pool, dev0, "empty")
     G.assert_host_equal(pool, host0, "empty")
 
 
 # ----------------------------------------------------- events gate a consumer
 
-@pytest.mark.parametrize("burst", BURSTS)
+@pytest.mark.parametrize("burst", BURSTS + ["staged"])
 def test_layer_events_gate_consumer_checksum(burst):
-    """A consumer on another stream waits on event l only, and must see layer l fully loaded."""
+    """A consumer on another stream waits on event l only, and must see layer l fully loaded.
+
+    The staged variant has room for 4 layers of every page, so its layers land
+    in groups of 1, 2, 4, 4 and 1.
+    """
     s = G.shape("mla", L=12, T=1, head_num=1, head_dim=576, dtype_size=2, P=64, slots=65536,
                 pages=512)
     pool = G.make_pool(s, 20)
@@ -648,8 +722,13 @@ def test_layer_events_gate_consumer_checksum(burst):
     load_stream = torch.cuda.Stream()
     torch.cuda.synchronize()
     opts = hk.Opts(burst_words=_burst_words(s.num_layers)) if burst == "single_launch" else None
+    ht_load, dt_load = ht, dt
+    if burst == "staged":
+        dt_load, ht_load = G.index_tensors(d, h, "host")
+        opts = _opts(hk.HICACHE_PATH_STAGED, "host",
+                     staging=_staging(4 * d.size * s.row_bytes))
     with torch.cuda.stream(load_stream):
-        hk.hicache_load_burst(pool, 0, s.num_layers, ht, dt, layer_done=events,
+        hk.hicache_load_burst(pool, 0, s.num_layers, ht_load, dt_load, layer_done=events,
                               stream=load_stream, opts=opts)
     for l in range(s.num_layers):
         consumer.wait_event(events[l])
