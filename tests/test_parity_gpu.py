@@ -123,6 +123,46 @@ def test_tiny_mha_backup_then_load(where, dtype, path):
             assert np.array_equal(a, b)
 
 
+@pytest.mark.parametrize("pages", [1, 63, 64, 65, 128, 129])
+@pytest.mark.parametrize("path", ["zero_copy", "zero_copy_single_launch", "staged"])
+def test_boundary_page_counts(pages, path):
+    """The page counts the pages' unit test probes, through the CUDA path.
+
+    The staging buffers hold exactly 64 pages of all layers, so 63/64/65 and
+    128/129 pages fall just inside, on and just past the staged path's chunk
+    boundaries (backup chunks of 64 pages; load groups of 1 and 2 layers in
+    chunks of 192 and 96 pages).
+    """
+    s = G.shape(L=3, T=2, head_num=2, head_dim=64, dtype_size=2, P=16, slots=16 * 300, pages=160)
+    pool = G.make_pool(s, seed=40 + pages)
+    P = s.page_size
+    d, h, dp, _ = W.page_pairs(41 + pages, pages, s.device_slots // P, s.host_pages, P)
+    where = "host" if path == "staged" else "device"
+    dev0, host0 = G.device_images(pool), G.host_images(pool)
+    dt, ht = G.index_tensors(d, h, where)
+    if path == "staged":
+        per_page = s.num_tensors * s.num_layers * P * s.row_bytes
+        opts = _opts(hk.HICACHE_PATH_STAGED, where, staging=_staging(64 * per_page))
+    elif path == "zero_copy_single_launch":
+        opts = _opts(hk.HICACHE_PATH_ZERO_COPY, where, burst_words=_burst_words(s.num_layers))
+    else:
+        opts = _opts(hk.HICACHE_PATH_ZERO_COPY, where)
+    hk.hicache_backup_all_layers(pool, dt, ht, opts=opts)
+    torch.cuda.synchronize()
+    G.oracle_backup(pool, dev0, host0, d, h)
+    G.assert_host_equal(pool, host0, f"{pages} pages backup")
+    d2, _, _, _ = W.page_pairs(42 + pages, pages, s.device_slots // P, s.host_pages, P,
+                               exclude_device_pages=dp)
+    d2t, _ = G.index_tensors(d2, h, where)
+    dev1 = G.device_images(pool)
+    events = [torch.cuda.Event() for _ in range(s.num_layers)]
+    _arm(events)
+    hk.hicache_load_burst(pool, 0, s.num_layers, ht, d2t, opts=opts, layer_done=events)
+    _assert_recorded_behind_sleep(events)
+    G.oracle_load(pool, dev1, host0, range(s.num_layers), h, d2)
+    G.assert_device_equal(pool, dev1, f"{pages} pages burst")
+
+
 # ------------------------------------------------------ ragged shapes and tails
 
 CASES = [
