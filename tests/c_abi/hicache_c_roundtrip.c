@@ -4,9 +4,10 @@
  * Test program: allocates a small MHA pool with the CUDA runtime (device layers
  * with cudaMalloc, the page-first host pool with cudaHostAlloc), backs up a
  * list of whole pages with hicache_backup_all_layers, loads them back into
- * other device pages with a single-launch hicache_load_burst, and checks every
- * byte of both pools against the CPU oracle (test infrastructure, linked only
- * by tests).  Exit status 0 means bit-exact; it prints the first mismatch
+ * other device pages with a single-launch hicache_load_burst, repeats both on
+ * the staged path with cudaMalloc'd staging buffers, and checks every byte of
+ * both pools against the CPU oracle (test infrastructure, linked only by
+ * tests).  Exit status 0 means bit-exact; it prints the first mismatch
  * otherwise.
  */
 #include <stdint.h>
@@ -180,6 +181,54 @@ int main(void) {
   if (hicache_load_burst(&pool, 1, 0, L, h_idx, d2_idx, 64, n, &opts, stream, ev) != HICACHE_EDUP)
     return 5;
   for (int l = 0; l < L; ++l) CHECK_CUDA(cudaEventSynchronize(ev[l]));
+
+  /* the staged path: backup to other host pages, then a burst into other
+     device pages.  The staging holds 7 host pages of all layers (backup in
+     chunks of 7 + 3 pages), 21 pages of one layer and 10 of two (load groups
+     of 1 and 2 layers, one chunk each). */
+  int64_t hpages3[NPAGES], dpages3[NPAGES];
+  sample(10, HPAGES, NPAGES, hpages, NPAGES, hpages3);
+  sample(11, SLOTS / P, NPAGES, dpages, NPAGES, dpages3);
+  for (int64_t k = 0; k < NPAGES; ++k)
+    for (int64_t t = 0; t < P; ++t) {
+      h_idx[k * P + t] = hpages3[k] * P + t;
+      d2_idx[k * P + t] = dpages3[k] * P + t;
+    }
+  const size_t stage_bytes = (size_t)7 * T * L * P * R;
+  void* staging[2];
+  for (int b = 0; b < 2; ++b) CHECK_CUDA(cudaMalloc(&staging[b], stage_bytes));
+  hicache_opts sopts;
+  memset(&sopts, 0, sizeof(sopts));
+  sopts.path = HICACHE_PATH_STAGED;
+  sopts.index_location = HICACHE_INDEX_HOST;
+  sopts.staging[0] = staging[0];
+  sopts.staging[1] = staging[1];
+  sopts.staging_bytes = stage_bytes;
+  CHECK_HK(hicache_backup_all_layers(&pool, 1, d_idx, h_idx, 64, n, &sopts, stream));
+  CHECK_HK(hicache_load_burst(&pool, 1, 0, L, h_idx, d2_idx, 64, n, &sopts, stream, ev));
+  CHECK_CUDA(cudaStreamSynchronize(stream));
+  for (int t = 0; t < T; ++t) {
+    uint8_t* layers[L];
+    for (int l = 0; l < L; ++l) layers[l] = dev_img[t * L + l];
+    if (oracle_backup_all_layers(L, P, R, SLOTS, HPAGES, (const uint8_t* const*)layers,
+                                 host_img[t], d_idx, h_idx, n) != 0)
+      return 4;
+    if (oracle_load_burst(L, P, R, SLOTS, HPAGES, 0, L, layers, host_img[t], h_idx, d2_idx, n) != 0)
+      return 4;
+    for (size_t b = 0; b < host_bytes; ++b)
+      if (host[t][b] != host_img[t][b]) {
+        fprintf(stderr, "staged backup: tensor %d byte %zu differs\n", t, b);
+        return 1;
+      }
+    for (int l = 0; l < L; ++l) {
+      CHECK_CUDA(cudaMemcpy(got, dev[t * L + l], layer_bytes, cudaMemcpyDeviceToHost));
+      for (size_t b = 0; b < layer_bytes; ++b)
+        if (got[b] != dev_img[t * L + l][b]) {
+          fprintf(stderr, "staged burst: tensor %d layer %d byte %zu differs\n", t, l, b);
+          return 1;
+        }
+    }
+  }
 
   printf("c abi round trip ok: %d layers, %d tensors, %d pages, launches %lld\n", L, T, NPAGES,
          (long long)hicache_kernel_launches());

@@ -502,9 +502,11 @@ def test_state_pools_with_multi_mib_rows(path):
 
 # ------------------------------------------------------- concurrent host threads
 
-def test_two_threads_burst_concurrently():
-    """Two host threads, each with its own stream, pool and burst words, run backups and
-    single-launch bursts at the same time; both results must match the oracle."""
+@pytest.mark.parametrize("path", ["zero_copy_single_launch", "staged"])
+def test_two_threads_burst_concurrently(path):
+    """Two host threads, each with its own stream, pool and burst words (or staging
+    buffers), run backups and bursts at the same time; both results must match the
+    oracle.  The staged buffers hold 2 layers of every page: groups 1, 2, 2, 1."""
     import threading
 
     s = G.shape("mla", L=6, T=1, head_num=1, head_dim=576, dtype_size=2, P=64, slots=64 * 64,
@@ -524,7 +526,11 @@ def test_two_threads_burst_concurrently():
             d, h = pairs[k][0], pairs[k][1]
             dt, ht = G.index_tensors(d, h, "host")
             d2t, _ = G.index_tensors(fresh[k], h, "host")
-            opts = _opts(hk.HICACHE_PATH_ZERO_COPY, "host", burst_words=_burst_words(6))
+            if path == "staged":
+                opts = _opts(hk.HICACHE_PATH_STAGED, "host",
+                             staging=_staging(2 * d.size * s.row_bytes))
+            else:
+                opts = _opts(hk.HICACHE_PATH_ZERO_COPY, "host", burst_words=_burst_words(6))
             for _ in range(3):
                 hk.hicache_backup_all_layers(pools[k], dt, ht, opts=opts, stream=stream)
                 hk.hicache_load_burst(pools[k], 0, 6, ht, d2t, opts=opts, stream=stream,
