@@ -205,7 +205,8 @@ hicache_status staged_backup(const std::vector<PoolInfo>& pools, const hicache_o
 // therefore copies a group of consecutive layers of each host page per DMA
 // (they are adjacent in a page-first host page) and lets the groups grow
 // 1, 2, 4, ... layers until one copy carries about this many bytes, so that
-// the first layer still lands after one layer's transfer.
+// the first layer still lands after one layer's transfer.  A 32-layer burst
+// runs as groups of 1, 2, 4, 8 and 17 layers.
 constexpr int64_t kDmaCopyTargetBytes = int64_t(4) << 20;
 // A group too large for the staging to hold every page at once moves in
 // chunks of pages; a chunk holds at least this many pages (or all of them),
@@ -254,9 +255,13 @@ hicache_status staged_load(const std::vector<PoolInfo>& pools, const hicache_opt
   int64_t step = 0;
   int32_t g_want = 1;
   for (int32_t l = layer_begin, g = 1; l < layer_end; l += g) {
-    // the largest group (up to g_want) whose chunks hold kMinChunkPages
-    // pages, or every page; one layer per group when not even that fits
+    // the next group size; a tail shorter than the group joins it rather
+    // than paying for small copies of its own
     g = std::min(g_want, layer_end - l);
+    const int32_t rest = layer_end - l - g;
+    if (rest > 0 && rest < g && g + rest <= g_cap) g += rest;
+    // the largest such group whose chunks hold kMinChunkPages pages, or every
+    // page; one layer per group when not even that fits
     while (g > 1 && layout_for(pools, o, g).cap_pages < std::min(groups, kMinChunkPages)) --g;
     g_want = std::min(g_cap, 2 * g_want);
     const StagingLayout lay = layout_for(pools, o, g);

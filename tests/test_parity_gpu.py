@@ -383,7 +383,7 @@ def test_page_first_layout_backup_then_load(where, path):
 STAGED_GROUP_CASES = [
     ("page_first_direct", 24, None, (0, 13)),   # groups 1, 2, 4, 6, one chunk each
     ("page_first_direct", 24, 3, (0, 13)),      # groups 1, 2, 3, 3, 3, 1
-    ("page_first_direct", 24, None, (2, 11)),   # groups 1, 2, 4, 2 from layer 2
+    ("page_first_direct", 24, None, (2, 11)),   # groups 1, 2, 6 from layer 2 (tail joins)
     ("page_first", 24, None, (0, 13)),
     ("page_first", 24, 3, (1, 12)),
     # 80 pages, room for 40 pages of 4 layers: groups 1, 2, 4, 5, 1; the group of
@@ -754,7 +754,7 @@ def test_layer_events_gate_consumer_checksum(burst):
     """A consumer on another stream waits on event l only, and must see layer l fully loaded.
 
     The staged variant has room for 4 layers of every page, so its layers land
-    in groups of 1, 2, 4, 4 and 1.
+    in groups of 1, 2, 4 and 5, the last in chunks of 204 and 52 pages.
     """
     s = G.shape("mla", L=12, T=1, head_num=1, head_dim=576, dtype_size=2, P=64, slots=65536,
                 pages=512)
