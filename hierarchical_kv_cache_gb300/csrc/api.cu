@@ -63,6 +63,21 @@ hicache_status device_view(const void* ptr, Want want, const std::string& what, 
   return HICACHE_OK;
 }
 
+// An optional buffer that kernels or stream operations write: NULL, or memory
+// of kind `want` whose address is a multiple of `align`.  On success *ptr
+// becomes its device-visible address.
+template <typename T>
+hicache_status check_gpu_buffer(T** ptr, Want want, size_t align, const std::string& what) {
+  if (!*ptr) return HICACHE_OK;
+  if (reinterpret_cast<uintptr_t>(*ptr) % align != 0)
+    return fail(HICACHE_EALIGN, what + " is not " + std::to_string(align) + "-byte aligned");
+  const void* v = nullptr;
+  const hicache_status st = device_view(*ptr, want, what, &v);
+  if (st != HICACHE_OK) return st;
+  *ptr = static_cast<T*>(const_cast<void*>(v));
+  return HICACHE_OK;
+}
+
 struct Prepared {
   std::vector<PoolInfo> pools;
   hicache_opts o{};
@@ -142,7 +157,17 @@ hicache_status prepare(const hicache_pool* pools, int32_t num_pools, const void*
   if (out->o.path == HICACHE_PATH_STAGED &&
       (!out->o.staging[0] || !out->o.staging[1] || out->o.staging_bytes == 0))
     return fail(HICACHE_ENOSTAGE, "staged path requested without two staging buffers");
-  return HICACHE_OK;
+  // The optional buffers the copy writes: a pointer of the wrong kind or
+  // alignment is an error status here, not a fault on the GPU later.
+  hicache_opts& o = out->o;
+  st = check_gpu_buffer(&o.device_error, Want::kAny, 4, "opts.device_error");
+  if (st == HICACHE_OK) st = check_gpu_buffer(&o.burst_words, Want::kDevice, 4, "opts.burst_words");
+  if (st == HICACHE_OK)
+    st = check_gpu_buffer(&o.index_staging, Want::kDevice, 16, "opts.index_staging");
+  for (int b = 0; b < 2 && st == HICACHE_OK; ++b)
+    st = check_gpu_buffer(&o.staging[b], Want::kDevice, 16,
+                          "opts.staging[" + std::to_string(b) + "]");
+  return st;
 }
 
 // Host-only checks of opts->burst_words for a burst of `count` layers.
@@ -364,6 +389,8 @@ extern "C" hicache_status hicache_layer_checksum(const hicache_pool* pool, int32
   if (n == 0) return HICACHE_OK;
   const void* v = nullptr;
   st = device_view(device_indices, Want::kDevice, "device_indices", &v);
+  if (st != HICACHE_OK) return st;
+  st = check_gpu_buffer(&out_sum, Want::kDevice, 8, "out_sum");
   if (st != HICACHE_OK) return st;
   return launch_checksum(pools[0], tensor, layer, v, index_bits, n, out_sum, stream);
 }

@@ -58,7 +58,10 @@
  *   the ABI.  hicache_last_error() returns a per-thread message for the last
  *   non-OK status.  Argument and index validation complete before any copy is
  *   enqueued, so a rejected call moves no byte.  A load call that fails still
- *   records every layer-done event it was given on `stream`.
+ *   records every layer-done event it was given on `stream`.  Buffers the GPU
+ *   writes (pool tensors, staging, opts.device_error, opts.burst_words,
+ *   opts.index_staging) are checked for alignment (HICACHE_EALIGN) and, except
+ *   the per-layer device pointers, for the kind of memory (HICACHE_EINVAL).
  */
 #ifndef HICACHE_H
 #define HICACHE_H
@@ -135,10 +138,11 @@ typedef struct hicache_opts {
   int32_t max_ctas;        /* 0 = library default; else caps the CTAs of each copy kernel so that
                               a concurrent consumer keeps the remaining SMs */
   int32_t reserved;        /* must be 0 */
-  void* staging[2];        /* staged path: two device buffers used alternately */
+  void* staging[2];        /* staged path: two device buffers used alternately, 16-byte aligned */
   size_t staging_bytes;    /* bytes of each staging buffer */
   cudaStream_t copy_stream;/* staged path: stream for the DMA copies (0 = library-internal) */
-  uint32_t* device_error;  /* optional device-accessible word; kernels OR HICACHE_DEVERR_* bits */
+  uint32_t* device_error;  /* optional word in device or pinned host memory, 4-byte aligned;
+                              kernels OR HICACHE_DEVERR_* bits into it */
   uint32_t* burst_words;   /* optional device memory of >= 4 words per burst layer: makes a
                               zero-copy hicache_load_burst one kernel launch for all its layers
                               (see hicache_load_burst); NULL = one launch per layer */

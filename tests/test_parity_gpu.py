@@ -726,6 +726,68 @@ def test_staged_burst_records_every_event_in_groups():
     G.assert_device_equal(pool, dev1, "staged groups")
 
 
+BAD_BUFFERS = ["staging_misaligned", "staging_pinned_host", "device_error_misaligned",
+               "device_error_pageable", "burst_words_pinned_host", "index_staging_pinned_host"]
+
+
+@pytest.mark.parametrize("case", BAD_BUFFERS)
+def test_bad_gpu_buffers_rejected_and_events_recorded(case):
+    """A buffer the GPU would write, of the wrong kind or alignment, is an error status.
+
+    Every case fails host-side validation, so nothing is launched; the load
+    still records its events and no byte moves.
+    """
+    s = G.shape(L=3, T=2, head_num=2, head_dim=64, dtype_size=2, P=16, slots=1024, pages=64)
+    pool = G.make_pool(s, 38)
+    dev0, host0 = G.device_images(pool), G.host_images(pool)
+    P = s.page_size
+    d, h, _, _ = W.page_pairs(39, 4, s.device_slots // P, s.host_pages, P)
+    where = "host" if case.startswith(("staging", "index_staging")) else "device"
+    dt, ht = G.index_tensors(d, h, where)
+    cuda8 = lambda n: torch.zeros(n, dtype=torch.uint8, device="cuda")  # noqa: E731
+    pinned8 = lambda n: torch.zeros(n, dtype=torch.uint8).pin_memory()  # noqa: E731
+    kw, want = {}, hk.HICACHE_EINVAL
+    path = hk.HICACHE_PATH_ZERO_COPY
+    if case == "staging_misaligned":
+        path, want = hk.HICACHE_PATH_STAGED, hk.HICACHE_EALIGN
+        kw["staging"] = [cuda8(1 << 20)[4:], cuda8(1 << 20)]
+    elif case == "staging_pinned_host":
+        path = hk.HICACHE_PATH_STAGED
+        kw["staging"] = [pinned8(1 << 20), pinned8(1 << 20)]
+    elif case == "device_error_misaligned":
+        want = hk.HICACHE_EALIGN
+        kw["device_error"] = cuda8(8)[2:6]
+    elif case == "device_error_pageable":
+        kw["device_error"] = torch.zeros(1, dtype=torch.int32)
+    elif case == "burst_words_pinned_host":
+        kw["burst_words"] = torch.zeros(4 * s.num_layers, dtype=torch.int32).pin_memory()
+    else:
+        kw["index_staging"] = pinned8(hk.index_staging_bytes(d.size, 64))
+    opts = _opts(path, where, **kw)
+    with pytest.raises(hk.HiCacheError) as ei:  # every call checks every buffer it is given
+        hk.hicache_backup_all_layers(pool, dt, ht, opts=opts)
+    assert ei.value.status == want, ei.value.message
+    events = [torch.cuda.Event() for _ in range(s.num_layers)]
+    _arm(events)
+    with pytest.raises(hk.HiCacheError) as ei:
+        hk.hicache_load_burst(pool, 0, s.num_layers, ht, dt, opts=opts, layer_done=events)
+    assert ei.value.status == want, ei.value.message
+    _assert_recorded_behind_sleep(events)
+    G.assert_device_equal(pool, dev0, f"{case}: rejected burst moved bytes")
+    G.assert_host_equal(pool, host0, f"{case}: rejected backup moved bytes")
+
+
+def test_checksum_output_must_be_device_memory():
+    s = G.shape(L=2, T=1, head_num=1, head_dim=64, dtype_size=2, P=4, slots=256, pages=16)
+    pool = G.make_pool(s, 39)
+    dt = torch.arange(8, dtype=torch.int64, device="cuda")
+    for out, want in ((torch.zeros(1, dtype=torch.int64).pin_memory(), hk.HICACHE_EINVAL),
+                      (torch.zeros(16, dtype=torch.uint8, device="cuda")[4:12], hk.HICACHE_EALIGN)):
+        with pytest.raises(hk.HiCacheError) as ei:
+            hk.hicache_layer_checksum(pool, 0, 1, dt, out)
+        assert ei.value.status == want, ei.value.message
+
+
 def test_empty_lists_record_events_and_move_nothing():
     s = G.shape(L=3, T=2, head_num=2, head_dim=64, dtype_size=2, P=16, slots=1024, pages=64)
     pool = G.make_pool(s, 19)
