@@ -24,6 +24,10 @@ constexpr int kMaxRowsPerTask = 128; // rows of one warp task (shared-memory off
 constexpr int64_t kTaskBytes = 2048; // target payload of one warp task
 constexpr int kMaxSegSmall = 8;     // per-layer launches: pools x tensors
 constexpr int kMaxSegLarge = 512;   // all-layer launches: pools x tensors x layers
+// A signalling launch hands out its tasks from a 32-bit counter that every warp
+// bumps once past the last task; launches are cut at layer boundaries so that
+// tasks plus claims stay far below 2^32 (2^30 tasks is about 2 TB of rows).
+constexpr int64_t kMaxSignalTasks = int64_t(1) << 30;
 
 // Direction of one launch.
 enum Dir : int32_t { kDevToPaged = 0, kPagedToDev = 1 };

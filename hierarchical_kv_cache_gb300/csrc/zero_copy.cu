@@ -8,13 +8,14 @@
 // thread"), or an HBM staging buffer with the same page-first structure (staged
 // path).
 //
-// Work decomposition: a warp task is up to 32 rows of one segment (one pool,
-// tensor and layer).  Lane r loads pair r of the task, checks it and turns it
-// into a source and a destination byte offset.  The task's rows are then
-// treated as one flat array of VEC-byte chunks: lane k of an iteration copies
-// chunk c0 + k, fetching the offsets of that chunk's row from the owning lane
-// with a shuffle.  Rows that are adjacent on both sides therefore produce
-// fully coalesced 512-byte warp accesses whatever the row size, which is how
+// Work decomposition: a warp task is about 2 KiB of one segment (one pool,
+// tensor and layer): up to 128 rows, or one 2 KiB part of a longer row.  Lane
+// r loads the pairs of rows r, r + 32, ..., checks them and writes each row's
+// source and destination byte offsets into the warp's table in shared memory.
+// The task's rows are then treated as one flat array of VEC-byte chunks: lane
+// k of an iteration copies chunk c0 + k, reading its row's offsets from the
+// table.  Rows that are adjacent on both sides therefore produce fully
+// coalesced 512-byte warp accesses whatever the row size, which is how
 // contiguous index runs are merged without any run table.
 #include <cuda_runtime.h>
 
@@ -167,10 +168,10 @@ hicache_status launch_rows(const std::vector<PoolInfo>& pools, const SideSpec& s
                     side.paged_tokens[p], side.rows_per_page[p], &prm.pool[p]);
       tasks_per_layer += int64_t(pools[p].T) * prm.pool[p].tasks_per_seg;
     }
-    // A signalling launch covers whole layers only, and counts a layer's tasks
-    // in one 32-bit word.
-    if (signal && tasks_per_layer >= (int64_t(1) << 32) - 1)
-      return fail(HICACHE_EINVAL, "single-launch burst: more than 2^32-2 tasks per layer");
+    // A signalling launch covers whole layers only and counts its tasks in
+    // 32-bit words; one layer must fit in one launch.
+    if (signal && tasks_per_layer > kMaxSignalTasks)
+      return fail(HICACHE_EINVAL, "single-launch burst: more than 2^30 tasks in one layer");
     const int cap = signal ? (maxseg / segs_per_layer) * segs_per_layer : maxseg;
     int nseg = 0;
     int64_t tasks = 0;
@@ -200,7 +201,8 @@ hicache_status launch_rows(const std::vector<PoolInfo>& pools, const SideSpec& s
       return st;
     };
     for (int32_t l = layer_begin; l < layer_end; ++l) {
-      if (nseg + segs_per_layer > cap) {
+      if (nseg + segs_per_layer > cap ||
+          (signal && nseg > 0 && tasks + tasks_per_layer > kMaxSignalTasks)) {
         const hicache_status st = flush(l);
         if (st != HICACHE_OK) return st;
       }
