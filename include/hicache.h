@@ -103,8 +103,11 @@ typedef enum hicache_index_location {
   /* Both index arrays are in device memory and may still be being written on
    * `stream`.  The CPU does not read them: kernels skip pairs that are out of
    * range (or, for a page-granular pool, not page-aligned) and OR an error bit
-   * into opts->device_error when given.  Distinct destinations are the caller's
-   * responsibility in this mode. */
+   * into opts->device_error when given.  Distinct destinations, and for a
+   * page-granular pool in the page_first_direct layout whole pages, are the
+   * caller's responsibility in this mode: such a pool moves one page row per
+   * page_size pairs, addressed by the first pair of the group alone (the
+   * others are not read), so a bad first pair skips the whole page. */
   HICACHE_INDEX_DEVICE = 1
 } hicache_index_location;
 

@@ -151,3 +151,121 @@ def test_random_case(seed):
     if c["l1"] > c["l0"]:
         assert any(not np.array_equal(a, b) for dv, db in zip(dev1, dev_before)
                    for per_a, per_b in zip(dv, db) for a, b in zip(per_a, per_b)), what
+
+
+REJECT_CASES = 48
+FAULTS = ["dup_destination", "out_of_range", "negative", "partial_page", "layer_range"]
+
+
+@pytest.mark.parametrize("seed", range(REJECT_CASES))
+def test_random_fault(seed):
+    """One planted fault in a random case.
+
+    Host-located indices: the call fails with the fault's status, records every
+    layer event (checked behind a sleep kernel), and moves no byte.
+    Device-located indices (out-of-range and negative entries only): the
+    kernels skip the bad pairs, flag them in the error word, and move every
+    other pair.
+    """
+    g, c = _draw(10_000 + seed)
+    L, P, k = c["L"], c["P"], c["k"]
+    fault = FAULTS[seed % len(FAULTS)]
+    on_device = c["where"] == "device" and fault in ("out_of_range", "negative")
+    where = "device" if on_device else "host"
+    path = c["path"]
+    if fault == "partial_page":
+        if P == 1:
+            fault = "dup_destination"
+        elif path != "staged" and not any(s["page_granular"] for s in c["shapes"]):
+            path = "staged"  # whole host pages are required there
+    slots = c["dev_pages"] * P
+    pools = [G.make_pool(G.shape(s["name"], L=L, T=s["T"], head_num=s["head_num"],
+                                 head_dim=s["head_dim"], dtype_size=s["dtype_size"], P=P,
+                                 slots=slots, pages=c["host_pages"],
+                                 page_granular=s["page_granular"], layout=s["layout"],
+                                 value_kind="uint8_uniform" if s["page_granular"]
+                                 else "bf16_normal"), seed=200 * seed + i)
+             for i, s in enumerate(c["shapes"])]
+    d, h, dp, _ = W.page_pairs(seed, k, c["dev_pages"], c["host_pages"], P)
+    d2, _, _, _ = W.page_pairs(seed + 1, k, c["dev_pages"], c["host_pages"], P,
+                               exclude_device_pages=dp)
+    d, h, d2 = d.copy(), h.copy(), d2.copy()
+    n = d.size
+    # on the device the bad pair starts a page: a page-granular pool in the
+    # direct layout reads only the first pair of each page
+    i = int(g.integers(0, k)) * P if on_device else int(g.integers(0, n))
+    l0, l1 = 0, L
+    want = hk.HICACHE_EINVAL
+    if fault == "dup_destination":
+        if n < 2:
+            d, h, d2 = np.r_[d, d], np.r_[h, h], np.r_[d2, d2]  # the same pair twice
+        else:
+            j = (i + 1 + int(g.integers(0, n - 1))) % n
+            h[j], d2[j] = h[i], d2[i]
+        want = hk.HICACHE_EDUP
+    elif fault == "out_of_range":
+        h[i] = c["host_pages"] * P + int(g.integers(0, 1000))
+        d2[i] = slots + int(g.integers(0, 1000))
+        want = hk.HICACHE_ERANGE
+    elif fault == "negative":
+        h[i] = -1 - int(g.integers(0, 1000))
+        d2[i] = -1
+        want = hk.HICACHE_ERANGE
+    elif fault == "partial_page":
+        d, h, d2 = d[:-1], h[:-1], d2[:-1]
+    else:
+        l0, l1 = int(g.integers(0, L)), L + 1 + int(g.integers(0, 3))
+    dtype = c["idx_dtype"]
+    dt, ht = G.index_tensors(d, h, where, dtype)
+    d2t, _ = G.index_tensors(d2, h, where, dtype)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kw = dict(device_error=err)
+    if path == "staged" and not on_device:
+        per_page = sum(p.num_tensors * L * P * p.row_bytes for p in pools)
+        kw["staging"] = [torch.empty(2 * per_page, dtype=torch.uint8, device="cuda")
+                         for _ in range(2)]
+        hpath = hk.HICACHE_PATH_STAGED
+    else:
+        hpath = hk.HICACHE_PATH_ZERO_COPY
+        if path == "single_launch":
+            kw["burst_words"] = torch.full((4 * (L + 3),), 7, dtype=torch.int32, device="cuda")
+    loc = hk.HICACHE_INDEX_DEVICE if on_device else hk.HICACHE_INDEX_HOST
+    opts = hk.Opts(path=hpath, index_location=loc, **kw)
+    what = f"seed {seed}: fault {fault}, path {path}, {c}"
+    imgs = [(G.device_images(p), G.host_images(p)) for p in pools]
+
+    if on_device:
+        hk.hicache_backup_all_layers(pools, dt, ht, opts=opts)
+        hk.hicache_load_burst(pools, 0, L, ht, d2t, opts=opts,
+                              layer_done=[torch.cuda.Event() for _ in range(L)])
+        torch.cuda.synchronize()
+        assert int(err.item()) == hk.HICACHE_DEVERR_RANGE, what
+        for s, p, (dev0, host0) in zip(c["shapes"], pools, imgs):
+            keep = np.ones(n, dtype=bool)
+            page_rows = s["page_granular"] and s["layout"] == "page_first_direct"
+            keep[i:i + P if page_rows else i + 1] = False
+            G.oracle_backup(p, dev0, host0, d[keep], h[keep])
+            G.assert_host_equal(p, host0, "backup " + what)
+            G.oracle_load(p, dev0, host0, range(L), h[keep], d2[keep])
+            G.assert_device_equal(p, dev0, "burst " + what)
+        return
+
+    if fault != "layer_range":
+        with pytest.raises(hk.HiCacheError) as ei:
+            hk.hicache_backup_all_layers(pools, dt, ht, opts=opts)
+        assert ei.value.status == want, what + " / " + ei.value.message
+    events = [torch.cuda.Event() for _ in range(max(0, l1 - l0))]
+    for e in events:
+        e.record()
+    torch.cuda.synchronize()
+    torch.cuda._sleep(200_000_000)
+    with pytest.raises(hk.HiCacheError) as ei:
+        hk.hicache_load_burst(pools, l0, l1, ht, d2t, opts=opts, layer_done=events)
+    assert ei.value.status == want, what + " / " + ei.value.message
+    assert not any(e.query() for e in events), "a layer event was not recorded: " + what
+    torch.cuda.synchronize()
+    assert all(e.query() for e in events)
+    assert int(err.item()) == 0, what
+    for p, (dev0, host0) in zip(pools, imgs):
+        G.assert_host_equal(p, host0, "rejected backup moved bytes: " + what)
+        G.assert_device_equal(p, dev0, "rejected burst moved bytes: " + what)
