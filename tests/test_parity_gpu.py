@@ -555,6 +555,47 @@ def test_two_threads_burst_concurrently(path):
         G.assert_device_equal(p, dev0, f"thread {k} burst")
 
 
+@pytest.mark.parametrize("burst", BURSTS)
+def test_device_indices_written_on_the_stream_are_read_in_order(burst):
+    """Device indices written on `stream` just before a call are the ones it uses.
+
+    The index tensors start out as out-of-range sentinels; the real indices are
+    copied into them on the stream behind a sleep kernel, right before each
+    call.  Reading them any earlier would see the sentinels, skip every pair
+    and set the error word.
+    """
+    s = G.shape(L=5, T=2, head_num=2, head_dim=64, dtype_size=2, P=16, slots=2048, pages=64)
+    pool = G.make_pool(s, 44)
+    P = s.page_size
+    d, h, dp, _ = W.page_pairs(45, 12, s.device_slots // P, s.host_pages, P)
+    d2, _, _, _ = W.page_pairs(46, 12, s.device_slots // P, s.host_pages, P,
+                               exclude_device_pages=dp)
+    dev0, host0 = G.device_images(pool), G.host_images(pool)
+    real = {k: torch.as_tensor(v).cuda() for k, v in (("d", d), ("h", h), ("d2", d2))}
+    idx = {k: torch.full_like(v, -(10 ** 9)) for k, v in real.items()}  # sentinels
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    opts = _opts(hk.HICACHE_PATH_ZERO_COPY, "device", device_error=err,
+                 burst_words=_burst_words(s.num_layers) if burst == "single_launch" else None)
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(100_000_000)
+        idx["d"].copy_(real["d"])
+        idx["h"].copy_(real["h"])
+        hk.hicache_backup_all_layers(pool, idx["d"], idx["h"], opts=opts, stream=stream)
+        torch.cuda._sleep(100_000_000)
+        idx["d2"].copy_(real["d2"])
+        hk.hicache_load_burst(pool, 0, s.num_layers, idx["h"], idx["d2"], opts=opts,
+                              stream=stream,
+                              layer_done=[torch.cuda.Event() for _ in range(s.num_layers)])
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0, "a call read its indices before the stream wrote them"
+    G.oracle_backup(pool, dev0, host0, d, h)
+    G.assert_host_equal(pool, host0, "backup")
+    G.oracle_load(pool, dev0, host0, range(s.num_layers), h, d2)
+    G.assert_device_equal(pool, dev0, "burst")
+
+
 # ----------------------------------------------------------------- error paths
 
 def test_device_indices_out_of_range_are_skipped_and_flagged():
