@@ -72,15 +72,18 @@ def _index_staging(n, dtype=torch.int64):
     return torch.empty(hk.index_staging_bytes(n, bits), dtype=torch.uint8, device="cuda")
 
 
-@pytest.mark.parametrize("where", ["device", "host", "host_staged_idx"])
+# the staged path plans its copies on the CPU, so it takes host-located indices only
+PATH_WHERE = [(p, w) for p in ("zero_copy", "staged", "zero_copy_single_launch")
+              for w in ("device", "host", "host_staged_idx")
+              if not (p == "staged" and w == "device")]
+
+
+@pytest.mark.parametrize("path,where", PATH_WHERE)
 @pytest.mark.parametrize("dtype", [torch.int32, torch.int64])
-@pytest.mark.parametrize("path", ["zero_copy", "staged", "zero_copy_single_launch"])
 def test_tiny_mha_backup_then_load(where, dtype, path):
     """host_staged_idx: host-located indices copied by the library into opts.index_staging."""
     wl = W.tiny_mha()
     s = wl.pools[0]
-    if path == "staged" and where == "device":
-        pytest.skip("the staged path plans DMA spans on the CPU: host-located indices only")
     extra = {}
     if where == "host_staged_idx":
         where = "host"
@@ -343,11 +346,8 @@ def test_indexer_rejects_partial_pages_on_device():
 
 # ------------------------------------------------------- page_first host layout
 
-@pytest.mark.parametrize("where", ["device", "host"])
-@pytest.mark.parametrize("path", ["zero_copy", "zero_copy_single_launch", "staged"])
+@pytest.mark.parametrize("path,where", [pw for pw in PATH_WHERE if pw[1] != "host_staged_idx"])
 def test_page_first_layout_backup_then_load(where, path):
-    if path == "staged" and where == "device":
-        pytest.skip("the staged path plans DMA spans on the CPU: host-located indices only")
     s = G.shape(L=5, T=2, head_num=2, head_dim=64, dtype_size=2, P=16, slots=4096, pages=96,
                 layout="page_first")
     pool = G.make_pool(s, seed=24)
