@@ -400,6 +400,7 @@ def run_ours(args, rank, world):
                               layer_done=warm_events)
         enq_idle.append(time.perf_counter() - t0)
     torch.cuda.synchronize()
+    host_s0 = measure_host_costs(hk, pools, d, h, dt_h, ht_h, d2t_h, L, opts, stream, n)
 
     K = args.steps
     ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
@@ -508,6 +509,7 @@ def run_ours(args, rank, world):
             "enqueue_us_per_layer": round(statistics.median(enq_idle) * 1e6 / L, 2),
             "enqueue_us_per_layer_queue_full": round(statistics.median(enq) * 1e6 / L, 2),
             "link_peak_gbs": {k: round(v, 2) for k, v in link.items()},
+            "host_s0": host_s0,
         },
         "roofline": None,  # filled below with the launch that dominates the step
         "roofline_backup": {
@@ -580,6 +582,53 @@ def run_ours(args, rank, world):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds)
     return res
+
+
+def measure_host_costs(hk, pools, d, h, dt_h, ht_h, d2t_h, L, opts, stream, n, reps=7):
+    """Host time of run planning and of whole calls with pinned host-located indices.
+
+    With host-located indices every call validates the pairs on the CPU (range,
+    distinct destinations, whole pages where needed) before it enqueues
+    anything.  Each call is issued on an idle stream, so the time is the call's
+    own host work, not a wait for a full launch queue; medians of `reps`.
+    """
+    import ctypes
+    import dataclasses
+
+    import torch
+    P = pools[0].page_size
+    dd = np.ascontiguousarray(d, dtype=np.int64)
+    hh = np.ascontiguousarray(h, dtype=np.int64)
+    count = ctypes.c_int64(0)
+    plan = []
+    for _ in range(reps):  # the C planner alone: it walks every pair
+        t0 = time.perf_counter()
+        st = hk.lib().hicache_plan_runs(dd.ctypes.data, hh.ctypes.data, 64, dd.size, P, None, 0,
+                                        ctypes.byref(count), None)
+        plan.append(time.perf_counter() - t0)
+        assert st == hk.HICACHE_OK
+    idx_staging = torch.empty(hk.index_staging_bytes(n, 64), dtype=torch.uint8, device="cuda")
+    o = dataclasses.replace(opts, index_location=hk.HICACHE_INDEX_HOST, index_staging=idx_staging)
+    events = [torch.cuda.Event() for _ in range(L)]
+    t_b, t_l = [], []
+    for _ in range(reps):
+        stream.synchronize()
+        t0 = time.perf_counter()
+        hk.hicache_backup_all_layers(pools, dt_h, ht_h, opts=o, stream=stream)
+        t_b.append(time.perf_counter() - t0)
+        stream.synchronize()
+        t0 = time.perf_counter()
+        hk.hicache_load_burst(pools, 0, L, ht_h, d2t_h, opts=o, stream=stream, layer_done=events)
+        t_l.append(time.perf_counter() - t0)
+    stream.synchronize()
+    return {"pairs": int(n),
+            "plan_runs_us": round(statistics.median(plan) * 1e6, 1),
+            "runs": int(count.value),
+            "backup_call_us_host_indices": round(statistics.median(t_b) * 1e6, 1),
+            "burst_call_us_host_indices": round(statistics.median(t_l) * 1e6, 1),
+            "note": "host wall time on an idle stream: the run planner over the op's pairs, "
+                    "and whole calls with pinned host indices (CPU validation, index copy to "
+                    "opts.index_staging, enqueue)"}
 
 
 def run_consumer_overlap(hk, pools, idx_l, opts, L, stream, bytes_layer, reps=5):

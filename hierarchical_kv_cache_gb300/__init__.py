@@ -27,6 +27,7 @@ from ._binding import (  # noqa: F401
     abi_version,
     hicache_backup_all_layers,
     hicache_backup_all_layers_static_staging,
+    hicache_check_pairs,
     hicache_layer_checksum,
     hicache_load_burst,
     hicache_load_layer,

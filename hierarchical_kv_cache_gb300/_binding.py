@@ -72,10 +72,11 @@ def lib():
         L.hicache_plan_runs.argtypes = [vp, vp, i32, i64, i32, ctypes.POINTER(c_run), i64,
                                         ctypes.POINTER(i64), ctypes.POINTER(i64)]
         L.hicache_layer_checksum.argtypes = [P, i32, i32, vp, i32, i64, vp, vp]
+        L.hicache_check_pairs.argtypes = [P, i32, vp, vp, i32, i64, i32]
         L.hicache_backup_all_layers_static_staging.argtypes = [P, i32, vp, vp, i32, i64, O, vp]
         L.hicache_backup_all_layers_static_staging.restype = ctypes.c_int
         for f in ("hicache_backup_all_layers", "hicache_load_layer", "hicache_load_burst",
-                  "hicache_plan_runs", "hicache_layer_checksum"):
+                  "hicache_plan_runs", "hicache_layer_checksum", "hicache_check_pairs"):
             getattr(L, f).restype = ctypes.c_int
         L.hicache_last_error.restype = ctypes.c_char_p
         L.hicache_last_error.argtypes = []
@@ -312,6 +313,20 @@ def hicache_plan_runs(device_indices, host_indices, page_size: int):
                                    count.value, ctypes.byref(count), ctypes.byref(full)))
     out = np.array([(r.d0, r.h0, r.len) for r in runs[:count.value]], dtype=np.int64)
     return out.reshape(-1, 3), full.value
+
+
+def hicache_check_pairs(pools, device_indices, host_indices, *, dest_is_device: bool) -> None:
+    """Host-only validation of a pair list in host memory, as a call with host-located
+    indices does it; raises HiCacheError with that call's status."""
+    arr, n, keep = _pools_arg(pools)
+    d = np.ascontiguousarray(device_indices)
+    h = np.ascontiguousarray(host_indices)
+    if d.dtype != h.dtype or d.dtype not in (np.int32, np.int64) or d.shape != h.shape:
+        raise TypeError("index arrays must be equal-length int32 or int64")
+    bits = 32 if d.dtype == np.int32 else 64
+    _check(lib().hicache_check_pairs(arr, n, d.ctypes.data, h.ctypes.data, bits, d.size,
+                                     int(bool(dest_is_device))))
+    del keep  # the pointer arrays lived until the call returned
 
 
 def hicache_layer_checksum(pool: Pool, tensor: int, layer: int, device_indices, out_sum, *,

@@ -373,6 +373,21 @@ extern "C" hicache_status hicache_plan_runs(const void* device_indices, const vo
                    num_runs, full_pages);
 }
 
+extern "C" hicache_status hicache_check_pairs(const hicache_pool* pools, int32_t num_pools,
+                                              const void* device_indices, const void* host_indices,
+                                              int32_t index_bits, int64_t n,
+                                              int32_t dest_is_device) {
+  clear_error();
+  std::vector<PoolInfo> checked;
+  hicache_status st = check_pools(pools, num_pools, &checked);
+  if (st != HICACHE_OK) return st;
+  if (dest_is_device != 0 && dest_is_device != 1)
+    return fail(HICACHE_EINVAL, "dest_is_device must be 0 or 1");
+  st = check_index_args(device_indices, host_indices, index_bits, n);
+  if (st != HICACHE_OK) return st;
+  return check_pairs_host(checked, device_indices, host_indices, index_bits, n, dest_is_device == 1);
+}
+
 extern "C" hicache_status hicache_layer_checksum(const hicache_pool* pool, int32_t tensor,
                                                  int32_t layer, const void* device_indices,
                                                  int32_t index_bits, int64_t n, uint64_t* out_sum,

@@ -43,24 +43,115 @@ void min_max(const T* p, int64_t n, int64_t* mn, int64_t* mx) {
   *mx = int64_t(hi);
 }
 
-// Sets one bit per value (all in range); returns the index of the first value
-// seen twice, or -1.  Leaves the bitmap all zero again either way.
+// End of the run that starts at pair i: the first j > i at which d or h does
+// not step by one from pair j - 1 (or n).  Differences are taken modulo 2^64,
+// which is defined for every value; a run that wraps past the largest int64 is
+// caught by the range check (its last value is below its first).  Blocks of 8
+// pairs are tested without branches, so a long run costs a fraction of a
+// nanosecond per pair, and a run of one pair a single comparison.
 template <typename T>
-int64_t mark_distinct(const T* p, int64_t n, uint64_t* bitmap) {
-  int64_t dup = -1, upto = n;
-  for (int64_t i = 0; i < n; ++i) {
-    const uint64_t x = uint64_t(p[i]);
-    const uint64_t bit = uint64_t(1) << (x & 63);
+int64_t run_end(const T* d, const T* h, int64_t i, int64_t n) {
+  auto steps = [&](int64_t j) {
+    return (uint64_t(int64_t(d[j])) - uint64_t(int64_t(d[j - 1])) - 1u) |
+           (uint64_t(int64_t(h[j])) - uint64_t(int64_t(h[j - 1])) - 1u);
+  };
+  int64_t j = i + 1;
+  if (j < n && steps(j) != 0) return j;
+  while (j + 8 <= n) {
+    uint64_t off = 0;
+    for (int u = 0; u < 8; ++u) off |= steps(j + u);
+    if (off != 0) break;
+    j += 8;
+  }
+  while (j < n && steps(j) == 0) ++j;
+  return j;
+}
+
+// Marks rows [x0, x0 + len) in the bitmap a word at a time.  Returns the first
+// row of the range that was already marked (nothing past it is marked then), or
+// -1.
+int64_t mark_range(uint64_t* bitmap, int64_t x0, int64_t len) {
+  const int64_t end = x0 + len;
+  for (int64_t x = x0; x < end;) {
+    const int b = int(x & 63);
+    const int64_t take = std::min<int64_t>(64 - b, end - x);
+    const uint64_t mask = (take == 64 ? ~uint64_t(0) : (uint64_t(1) << take) - 1) << b;
     uint64_t& w = bitmap[x >> 6];
-    if (w & bit) {
-      dup = i;
-      upto = i;
+    if (w & mask) return (x & ~int64_t(63)) + __builtin_ctzll(w & mask);
+    w |= mask;
+    x += take;
+  }
+  return -1;
+}
+
+// Result of the run pass over a pair list.
+struct RunCheck {
+  bool out_of_range = false;  // some pair addresses no row (named by a second walk)
+  int64_t dup_pair = -1;      // first pair whose destination was already named
+  int64_t dup_row = -1;       // that destination
+  int64_t bad_page = -1;      // first pair that breaks the whole-page structure
+  bool bad_start = false;     // ... because its page does not start page-aligned
+};
+
+// One pass over the runs of the pair list (maximal stretches where both sides
+// step by one).  Within a run the indices grow by one, so its first and last
+// pairs decide its range.  Destinations are marked in the bitmap run by run;
+// after the first duplicate only ranges are still checked, since a range error
+// takes precedence.  With `pages` every run must start a page in pair order and
+// page-aligned on both sides, which is exactly "every group of P pairs is one
+// whole aligned page" once n is a multiple of P.  The bitmap is left all zero.
+template <typename T>
+RunCheck check_runs(const T* d, const T* h, int64_t n, bool dest_is_device, bool pages, int64_t P,
+                    int64_t dev_lim, int64_t host_lim, uint64_t* bitmap) {
+  const T* dst = dest_is_device ? d : h;
+  RunCheck rc;
+  int64_t marked_end = 0;  // pairs [0, marked_end) may have marked words
+  int64_t lo = std::numeric_limits<int64_t>::max(), hi = -1;  // destinations marked
+  for (int64_t i = 0; i < n;) {
+    const int64_t e = run_end(d, h, i, n);
+    const int64_t d0 = int64_t(d[i]), d1 = int64_t(d[e - 1]);
+    const int64_t h0 = int64_t(h[i]), h1 = int64_t(h[e - 1]);
+    if (d0 < 0 || d1 >= dev_lim || d1 < d0 || h0 < 0 || h1 >= host_lim || h1 < h0) {
+      rc.out_of_range = true;
       break;
     }
-    w |= bit;
+    if (pages && rc.bad_page < 0) {
+      if (i % P != 0) {
+        rc.bad_page = i;
+      } else if (d0 % P != 0 || h0 % P != 0) {
+        rc.bad_page = i;
+        rc.bad_start = true;
+      }
+    }
+    if (rc.dup_pair < 0) {
+      const int64_t x0 = dest_is_device ? d0 : h0;
+      int64_t hit = -1;
+      if (e == i + 1) {  // a run of one pair: one bit
+        uint64_t& w = bitmap[x0 >> 6];
+        const uint64_t bit = uint64_t(1) << (x0 & 63);
+        if (w & bit) hit = x0;
+        w |= bit;
+      } else {
+        hit = mark_range(bitmap, x0, e - i);
+      }
+      marked_end = e;
+      lo = std::min(lo, x0);
+      hi = std::max(hi, x0 + (e - i) - 1);
+      if (hit >= 0) {
+        rc.dup_pair = i + (hit - x0);
+        rc.dup_row = hit;
+      }
+    }
+    i = e;
   }
-  for (int64_t i = 0; i < upto; ++i) bitmap[uint64_t(p[i]) >> 6] = 0;
-  return dup;
+  // Clear what was marked: every word of [lo, hi] when that is no more words
+  // than pairs, else the word of each pair marked.
+  if (hi >= lo && (hi >> 6) - (lo >> 6) + 1 <= n) {
+    std::fill(bitmap + (lo >> 6), bitmap + (hi >> 6) + 1, uint64_t(0));
+  } else {
+    for (int64_t j = 0; j < marked_end; ++j) bitmap[int64_t(dst[j]) >> 6] = 0;
+  }
+  return rc;
 }
 }  // namespace
 
@@ -158,18 +249,10 @@ hicache_status check_pairs_host(const std::vector<PoolInfo>& pools, const void* 
     host_lim = std::min(host_lim, p.host_pages * int64_t(p.P));
     any_page = any_page || p.page_granular;
   }
-  // Range: every pair must address a row of every pool of the call.  A
-  // min/max pass (which the compiler vectorises) decides; only a failing call
-  // walks the pairs again to name the first offender.
-  int64_t dmin, dmax, hmin, hmax;
-  if (bits == 32) {
-    min_max(static_cast<const int32_t*>(dev_idx), n, &dmin, &dmax);
-    min_max(static_cast<const int32_t*>(host_idx), n, &hmin, &hmax);
-  } else {
-    min_max(static_cast<const int64_t*>(dev_idx), n, &dmin, &dmax);
-    min_max(static_cast<const int64_t*>(host_idx), n, &hmin, &hmax);
-  }
-  if (dmin < 0 || dmax >= dev_lim || hmin < 0 || hmax >= host_lim) {
+  const void* dst = dest_is_device ? dev_idx : host_idx;
+  const int64_t lim = dest_is_device ? dev_lim : host_lim;
+  // Names the first pair that addresses no row of every pool of the call.
+  auto range_error = [&]() {
     for (int64_t i = 0; i < n; ++i) {
       const int64_t d = idx(dev_idx, bits, i);
       const int64_t h = idx(host_idx, bits, i);
@@ -178,13 +261,20 @@ hicache_status check_pairs_host(const std::vector<PoolInfo>& pools, const void* 
       if (h < 0 || h >= host_lim)
         return fail(HICACHE_ERANGE, "host index " + str(h) + " at pair " + str(i) + " outside [0, " + str(host_lim) + ")");
     }
-  }
-  // Distinct destinations: a bitmap over the destination rows, cleared again
-  // after use so that the cost stays O(n) per call.
-  const void* dst = dest_is_device ? dev_idx : host_idx;
-  const int64_t lim = dest_is_device ? dev_lim : host_lim;
+    return fail(HICACHE_ERANGE, "index out of range");  // not reached
+  };
   if (lim > (int64_t(1) << 28) && lim / 64 > 4 * n) {
-    // Sparse use of a huge destination space: sort a copy instead of a bitmap.
+    // Sparse use of a huge destination space: a min/max pass for the range,
+    // then distinct destinations by sorting a copy instead of a bitmap.
+    int64_t dmin, dmax, hmin, hmax;
+    if (bits == 32) {
+      min_max(static_cast<const int32_t*>(dev_idx), n, &dmin, &dmax);
+      min_max(static_cast<const int32_t*>(host_idx), n, &hmin, &hmax);
+    } else {
+      min_max(static_cast<const int64_t*>(dev_idx), n, &dmin, &dmax);
+      min_max(static_cast<const int64_t*>(host_idx), n, &hmin, &hmax);
+    }
+    if (dmin < 0 || dmax >= dev_lim || hmin < 0 || hmax >= host_lim) return range_error();
     std::vector<int64_t> v(static_cast<size_t>(n));
     for (int64_t i = 0; i < n; ++i) v[size_t(i)] = idx(dst, bits, i);
     std::sort(v.begin(), v.end());
@@ -194,17 +284,32 @@ hicache_status check_pairs_host(const std::vector<PoolInfo>& pools, const void* 
                                       str(v[i]) + " named twice");
     return check_whole_pages(any_page, P, dev_idx, host_idx, bits, n);
   }
+  // Range, distinct destinations (a bitmap over the destination rows, cleared
+  // again after use so that the cost stays O(n) per call) and whole pages, in
+  // one pass over the runs of the pair list.
   static thread_local std::vector<uint64_t> bitmap;
   const size_t words = size_t((lim + 63) / 64);
   if (bitmap.size() < words) bitmap.assign(words, 0);
-  const int64_t first_dup = bits == 32
-      ? mark_distinct(static_cast<const int32_t*>(dst), n, bitmap.data())
-      : mark_distinct(static_cast<const int64_t*>(dst), n, bitmap.data());
-  if (first_dup >= 0)
+  const RunCheck rc = bits == 32
+      ? check_runs(static_cast<const int32_t*>(dev_idx), static_cast<const int32_t*>(host_idx), n,
+                   dest_is_device, any_page, P, dev_lim, host_lim, bitmap.data())
+      : check_runs(static_cast<const int64_t*>(dev_idx), static_cast<const int64_t*>(host_idx), n,
+                   dest_is_device, any_page, P, dev_lim, host_lim, bitmap.data());
+  if (rc.out_of_range) return range_error();
+  if (rc.dup_pair >= 0)
     return fail(HICACHE_EDUP, std::string(dest_is_device ? "device" : "host") + " destination " +
-                                  str(idx(dst, bits, first_dup)) + " named twice (second time at pair " +
-                                  str(first_dup) + ")");
-  return check_whole_pages(any_page, P, dev_idx, host_idx, bits, n);
+                                  str(rc.dup_row) + " named twice (second time at pair " +
+                                  str(rc.dup_pair) + ")");
+  if (any_page && n % P != 0)
+    return fail(HICACHE_EINVAL, "page-granular pool: n=" + str(n) + " is not a multiple of page_size " + str(P));
+  if (rc.bad_page >= 0) {
+    const int64_t k = rc.bad_page / P * P;
+    if (rc.bad_start)
+      return fail(HICACHE_EINVAL, "page-granular pool: pair " + str(k) + " does not start a page");
+    return fail(HICACHE_EINVAL, "page-granular pool: pairs " + str(k) + ".." + str(k + P - 1) +
+                                    " are not one whole page");
+  }
+  return HICACHE_OK;
 }
 
 hicache_status check_whole_pages(bool any_page, int64_t P, const void* dev_idx, const void* host_idx,
@@ -236,23 +341,25 @@ hicache_status plan_runs(const void* dev_idx, const void* host_idx, int32_t bits
   if (cap < 0) return fail(HICACHE_EINVAL, "runs_cap is negative");
   const int64_t P = page_size;
   int64_t count = 0, full = 0;
-  int64_t i = 0;
-  while (i < n) {
-    const int64_t d0 = idx(dev_idx, bits, i);
-    const int64_t h0 = idx(host_idx, bits, i);
-    int64_t len = 1;
-    // extend while both sides step by one and the host side stays in its page
-    while (i + len < n) {
-      const int64_t d = idx(dev_idx, bits, i + len);
-      const int64_t h = idx(host_idx, bits, i + len);
-      if (d != d0 + len || h != h0 + len || h % P == 0) break;
-      ++len;
+  // Maximal stretches where both sides step by one, cut where the host slot
+  // starts a new page.
+  auto plan = [&](const auto* d, const auto* h) {
+    for (int64_t i = 0; i < n;) {
+      const int64_t e = run_end(d, h, i, n);
+      for (int64_t s = i; s < e;) {
+        const int64_t h0 = int64_t(h[s]);
+        const int64_t to_page_end = P - ((h0 % P) + P) % P;  // pairs left in h0's page
+        const int64_t len = std::min(e - s, to_page_end);
+        if (runs && count < cap) runs[count] = hicache_run{int64_t(d[s]), h0, len};
+        if (len == P && h0 % P == 0) ++full;
+        ++count;
+        s += len;
+      }
+      i = e;
     }
-    if (runs && count < cap) runs[count] = hicache_run{d0, h0, len};
-    if (len == P && h0 % P == 0) ++full;
-    ++count;
-    i += len;
-  }
+  };
+  if (bits == 32) plan(static_cast<const int32_t*>(dev_idx), static_cast<const int32_t*>(host_idx));
+  else plan(static_cast<const int64_t*>(dev_idx), static_cast<const int64_t*>(host_idx));
   *num_runs = count;
   if (full_pages) *full_pages = full;
   return HICACHE_OK;

@@ -75,7 +75,7 @@
 extern "C" {
 #endif
 
-#define HICACHE_ABI_VERSION 3
+#define HICACHE_ABI_VERSION 4 /* 4: adds hicache_check_pairs */
 
 typedef enum hicache_status {
   HICACHE_OK = 0,
@@ -282,6 +282,29 @@ hicache_status hicache_plan_runs(const void* device_indices, const void* host_in
                                  int32_t index_bits, int64_t n, int32_t page_size,
                                  hicache_run* runs_out, int64_t runs_cap, int64_t* num_runs,
                                  int64_t* full_pages);
+
+/*
+ * Index validation alone (host only; no CUDA call): checks n pairs in host
+ * memory against the pools exactly as a call with HICACHE_INDEX_HOST does
+ * before it enqueues anything, and returns the status that call would return
+ * for them.  In order of precedence:
+ *   HICACHE_ERANGE - a device index outside [0, device_slots) or a host index
+ *                    outside [0, host_pages * page_size) of some pool;
+ *   HICACHE_EDUP   - a destination named twice: host slots when
+ *                    dest_is_device is 0 (a backup), device slots when it is 1
+ *                    (a load);
+ *   HICACHE_EINVAL - for a page-granular pool, pairs that are not whole
+ *                    page-aligned pages (n a multiple of page_size, every group
+ *                    of page_size pairs one aligned page on both sides).
+ * The pools are checked as by every call (HICACHE_EINVAL / HICACHE_EALIGN).
+ * Lets a scheduler validate a pair list on its own thread, ahead of the call;
+ * the cost is one pass over the runs of the list (about a nanosecond per pair
+ * for lists of whole pages).
+ * Passage: sglang PR #38472, Motivation (the per-layer CPU work this replaces).
+ */
+hicache_status hicache_check_pairs(const hicache_pool* pools, int32_t num_pools,
+                                   const void* device_indices, const void* host_indices,
+                                   int32_t index_bits, int64_t n, int32_t dest_is_device);
 
 /*
  * Synthetic consumer (not a transfer): adds, over the pairs' device slots

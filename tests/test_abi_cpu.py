@@ -36,7 +36,7 @@ def test_header_symbols_exported():
     lib = ctypes.CDLL(B.LIB_PATH)
     missing = [n for n in names if not hasattr(lib, n)]
     assert not missing, f"declared but not exported: {missing}"
-    assert hk.abi_version() == 3
+    assert hk.abi_version() == 4
 
 
 def brute_runs(d, h, P):
