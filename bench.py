@@ -65,6 +65,8 @@ def parse_args():
                     help="override the pages moved per op (smaller profiling cases)")
     ap.add_argument("--device-slots", type=int, default=0, help="override device slots per pool")
     ap.add_argument("--host-pages", type=int, default=0, help="override host pages per pool")
+    ap.add_argument("--layout", choices=["page_first_direct", "page_first"], default=None,
+                    help="override the host layout of every pool of the workload")
     ap.add_argument("--sweep", action="store_true",
                     help="run the row-size / page-size / length / fragmentation sweep instead")
     ap.add_argument("--sweep-rows", default="16,64,256,1152,2048")
@@ -308,6 +310,10 @@ def build_workload(name, seed_offset=0, args=None):
 
     from hierarchical_kv_cache_gb300 import workloads as W
     wl = W.WORKLOADS[name]()
+    if args is not None and args.layout:
+        wl = dataclasses.replace(wl, pools=tuple(dataclasses.replace(s, layout=args.layout)
+                                                 for s in wl.pools),
+                                 name=wl.name + f" [host layout {args.layout}]")
     if args is not None and (args.pages or args.device_slots or args.host_pages):
         pools = tuple(dataclasses.replace(
             s, device_slots=args.device_slots or s.device_slots,
