@@ -72,6 +72,7 @@ def parse_args():
     ap.add_argument("--sweep-rows", default="16,64,256,1152,2048")
     ap.add_argument("--sweep-pages", default="1,16,64,256")
     ap.add_argument("--sweep-tokens", default="1024,4096,16384,65536,262144")
+    ap.add_argument("--sweep-layers", type=int, default=4)
     ap.add_argument("--dma-sweep", action="store_true",
                     help="measure the copy engine's cost per copy against the copy size instead")
     return ap.parse_args()
@@ -938,7 +939,7 @@ def run_sweep(args):
     rows = [int(x) for x in args.sweep_rows.split(",")]
     psizes = [int(x) for x in args.sweep_pages.split(",")]
     tokens = [int(x) for x in args.sweep_tokens.split(",")]
-    L = 4
+    L = args.sweep_layers
     link = measure_link_peak()
     stream = torch.cuda.Stream()
     staging = [torch.empty(args.staging_mib << 20, dtype=torch.uint8, device="cuda")
@@ -956,7 +957,9 @@ def run_sweep(args):
         for P in psizes:
             pool = Pool(device_layers=dev, host_tensors=host, num_layers=L, head_num=1,
                         head_dim=R // 2, dtype_size=2, page_size=P, device_slots=slots,
-                        host_pages=slots // P)
+                        host_pages=slots // P,
+                        layout=(hk.HICACHE_LAYOUT_PAGE_FIRST if args.layout == "page_first"
+                                else hk.HICACHE_LAYOUT_PAGE_FIRST_DIRECT))
             for n in tokens:
                 for frag in (False, True):
                     d, h = W.token_pairs(1000 + n + P, n, slots, slots, P, fragmented=frag)
@@ -992,6 +995,7 @@ def run_sweep(args):
                             rec = {"row_bytes": R, "page_size": P, "tokens": n,
                                    "fragmented": frag, "runs": int(len(runs)),
                                    "direction": direction, "path": path, "layers": L,
+                                   "layout": args.layout or "page_first_direct",
                                    "burst": args.burst if path == "zero_copy" else "per_layer",
                                    "ms": round(t, 4), "gbs": round(gbs, 2),
                                    "frac_of_link": round(gbs / peak, 4)}

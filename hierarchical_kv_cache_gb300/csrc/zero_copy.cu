@@ -23,6 +23,7 @@
 #include <atomic>
 #include <type_traits>
 #include <mutex>
+#include <numeric>
 #include <string>
 
 #include "consumer_kernel.cuh"
@@ -135,8 +136,17 @@ void fill_geometry(const PoolInfo& pi, int64_t npairs, int vec, int64_t paged_pa
   g->qS = uint32_t(32 * kUnroll) / g->cpr;
   g->rS = uint32_t(32 * kUnroll) % g->cpr;
   // about kTaskBytes per task: 128 rows of 16 B, one row of 2 KiB, or one
-  // 2 KiB part of a longer row (a state slot of several MiB, a long page row)
-  const int64_t rpt = (kTaskBytes + R - 1) / R;
+  // 2 KiB part of a longer row (a state slot of several MiB, a long page row).
+  // The row count is rounded up so that a task spans whole 128-byte lines when
+  // its rows are contiguous (a run of whole pages starts on a line): a line
+  // that two warps write at different times reaches the host in two partial
+  // writes.  Rows whose bytes already fill lines (2 KiB, 1152 B) keep their count.
+  int64_t rpt = (kTaskBytes + R - 1) / R;
+  if (R <= kTaskBytes) {
+    const int64_t line_rows = 128 / std::gcd(R, int64_t(128));  // rows that fill whole lines
+    const int64_t rounded = (rpt + line_rows - 1) / line_rows * line_rows;
+    if (rounded <= kMaxRowsPerTask) rpt = rounded;
+  }
   g->rows_per_task = int32_t(std::min<int64_t>(kMaxRowsPerTask, std::max<int64_t>(1, rpt)));
   g->part_chunks = uint32_t(kTaskBytes / vec);
   g->parts_per_row = R > kTaskBytes ? int32_t((g->cpr + g->part_chunks - 1) / g->part_chunks) : 1;
