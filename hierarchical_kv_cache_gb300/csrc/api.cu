@@ -78,6 +78,18 @@ hicache_status check_gpu_buffer(T** ptr, Want want, size_t align, const std::str
   return HICACHE_OK;
 }
 
+// True when `ptr` is device memory the CPU must not read.  When the query
+// itself fails (no usable device, or memory CUDA does not know) it cannot be
+// device memory of this process.
+bool is_device_memory(const void* ptr) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeDevice;
+}
+
 struct Prepared {
   std::vector<PoolInfo> pools;
   hicache_opts o{};
@@ -133,6 +145,10 @@ hicache_status prepare(const hicache_pool* pools, int32_t num_pools, const void*
   out->idx.bits = bits;
   out->idx.n = n;
   if (out->o.index_location == HICACHE_INDEX_HOST) {
+    // The CPU reads host-located indices next: they must not be device memory.
+    if (n > 0 && (is_device_memory(dev_idx) || is_device_memory(host_idx)))
+      return fail(HICACHE_EINVAL, "index_location is HICACHE_INDEX_HOST but an index array is "
+                                  "device memory");
     out->idx.dev_cpu = dev_idx;
     out->idx.host_cpu = host_idx;
     st = check_pairs_host(out->pools, dev_idx, host_idx, bits, n, dest_is_device);

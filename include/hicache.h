@@ -98,7 +98,9 @@ typedef enum hicache_path {
 typedef enum hicache_index_location {
   /* Both index arrays are in pinned (page-locked) host memory: the CPU validates
    * them completely before enqueueing (range, duplicate destinations, whole
-   * pages) and the GPU reads them through their mapping. */
+   * pages) and the GPU reads them through their mapping (or from
+   * opts->index_staging).  Device memory passed here is rejected with
+   * HICACHE_EINVAL before the CPU reads it. */
   HICACHE_INDEX_HOST = 0,
   /* Both index arrays are in device memory and may still be being written on
    * `stream`.  The CPU does not read them: kernels skip pairs that are out of

@@ -818,6 +818,26 @@ def test_bad_gpu_buffers_rejected_and_events_recorded(case):
     G.assert_host_equal(pool, host0, f"{case}: rejected backup moved bytes")
 
 
+def test_host_located_indices_in_device_memory_are_rejected():
+    """The CPU validates host-located indices, so they must not be device memory."""
+    s = G.shape(L=3, T=1, head_num=1, head_dim=64, dtype_size=2, P=4, slots=256, pages=16)
+    pool = G.make_pool(s, 47)
+    dev0, host0 = G.device_images(pool), G.host_images(pool)
+    dt, ht = G.index_tensors(np.arange(8), np.arange(8) + 16, "device")
+    opts = _opts(hk.HICACHE_PATH_ZERO_COPY, "host")  # declared host-located
+    with pytest.raises(hk.HiCacheError) as ei:
+        hk.hicache_backup_all_layers(pool, dt, ht, opts=opts)
+    assert ei.value.status == hk.HICACHE_EINVAL and "device memory" in ei.value.message
+    events = [torch.cuda.Event() for _ in range(3)]
+    _arm(events)
+    with pytest.raises(hk.HiCacheError) as ei:
+        hk.hicache_load_burst(pool, 0, 3, ht, dt, opts=opts, layer_done=events)
+    assert ei.value.status == hk.HICACHE_EINVAL
+    _assert_recorded_behind_sleep(events)
+    G.assert_device_equal(pool, dev0, "rejected burst moved bytes")
+    G.assert_host_equal(pool, host0, "rejected backup moved bytes")
+
+
 def test_checksum_output_must_be_device_memory():
     s = G.shape(L=2, T=1, head_num=1, head_dim=64, dtype_size=2, P=4, slots=256, pages=16)
     pool = G.make_pool(s, 39)
