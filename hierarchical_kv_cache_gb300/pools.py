@@ -7,7 +7,7 @@ from __future__ import annotations
 
 import torch
 
-from ._binding import Pool
+from ._binding import HICACHE_LAYOUT_PAGE_FIRST, HICACHE_LAYOUT_PAGE_FIRST_DIRECT, Pool
 
 
 def allocate_pool(shape, device: str = "cuda", pin_host: bool = True) -> Pool:
@@ -22,7 +22,9 @@ def allocate_pool(shape, device: str = "cuda", pin_host: bool = True) -> Pool:
                 head_dim=shape.head_dim, dtype_size=shape.dtype_size, page_size=shape.page_size,
                 device_slots=shape.device_slots, host_pages=shape.host_pages,
                 page_granular=bool(shape.page_granular),
-                layout=1 if getattr(shape, "layout", "page_first_direct") == "page_first" else 0)
+                layout=(HICACHE_LAYOUT_PAGE_FIRST
+                        if getattr(shape, "layout", "page_first_direct") == "page_first"
+                        else HICACHE_LAYOUT_PAGE_FIRST_DIRECT))
 
 
 def fill_device_random_(pool: Pool, seed: int, kind: str = "bf16_normal") -> None:
