@@ -52,6 +52,15 @@ struct PoolGeom {
   uint32_t vec;              // chunk bytes: 16, or 4 when a row or base is not 16-aligned
   int32_t parts_per_row;     // > 1: a row longer than a task is split into this many tasks
   uint32_t part_chunks;      // chunks of one such part (the last part may be shorter)
+  // Layer rows (all-layer backup into a token-major host pool): a task moves
+  // layers [k * rows_per_task, ...) of one token, whose layers are adjacent on
+  // the host, so that its host writes cover whole lines.  Its rows are layers;
+  // every task of the (pool, tensor) belongs to its layer-0 segment, and layer
+  // l's device buffer is the one of segment (that segment + l * seg_stride).
+  int32_t layer_rows;        // 1 = this mode
+  int32_t num_layers;        // L (layer rows only)
+  int32_t seg_stride;        // segments from one layer to the next (layer rows only)
+  int32_t tasks_per_token;   // ceil(L / rows_per_task) (layer rows only)
 };
 
 // One (pool, tensor, layer) stream.

@@ -52,7 +52,8 @@ __device__ __forceinline__ void flush_layer(const CopyParams<MAXSEG>& p, int lay
 
 // Copies the flat chunk range [chunk0, chunk0 + total) of one warp task, where
 // chunk c is chunk c % cpr of task row c / cpr.  offs[r] holds the source and
-// destination byte offsets of task row r (x < 0 marks a skipped row); (r, j)
+// destination byte offsets of task row r (y < 0 marks a skipped row: a
+// destination offset is never negative, a source offset may be); (r, j)
 // is the (row, chunk-in-row) position of chunk chunk0 + c0 + lane and advances
 // by precomputed quotients, so the loop has no division.
 template <typename V, int VEC>
@@ -71,7 +72,7 @@ __device__ __forceinline__ void copy_chunks(const longlong2* offs, const char* s
       dpos[u] = -1;
       if (c0 + uint32_t(lane) + 32u * u < total) {
         const longlong2 o = offs[rr];
-        if (o.x >= 0) {
+        if (o.y >= 0) {
           dpos[u] = o.y + int64_t(jj) * VEC;
           v[u] = ld_stream(reinterpret_cast<const V*>(src + o.x + int64_t(jj) * VEC));
         }
@@ -94,7 +95,7 @@ __device__ __forceinline__ void copy_chunks(const longlong2* offs, const char* s
 // Copies the rows of one warp task and returns the task's launch-relative
 // segment.  Called by all 32 lanes of a warp; offs is the warp's table of
 // kMaxRowsPerTask entries in shared memory.
-template <typename IdxT, int MAXSEG>
+template <typename IdxT, int MAXSEG, bool LAYER_ROWS>
 __device__ __forceinline__ int copy_task(const CopyParams<MAXSEG>& p, int64_t task, int lane,
                                          longlong2* offs) {
   // segment of this task: last s with seg_task_begin[s] <= task
@@ -105,8 +106,33 @@ __device__ __forceinline__ int copy_task(const CopyParams<MAXSEG>& p, int64_t ta
   }
   const Segment sg = p.seg[lo];
   const PoolGeom& g = p.pool[sg.pool];
-  // A task is rows_per_task whole rows, or one part of a row longer than a task.
   const int64_t t = task - p.seg_task_begin[lo];
+  if (LAYER_ROWS && g.layer_rows) {
+    // Layers [l0, l0 + nr) of one token: row r is layer l0 + r, read from that
+    // layer's own segment and written to the token's adjacent host rows.
+    const int64_t tok = t / g.tasks_per_token;
+    const int l0 = int(t - tok * g.tasks_per_token) * g.rows_per_task;
+    const int nr = min(g.rows_per_task, g.num_layers - l0);
+    const int64_t pair = p.pair_begin + tok;
+    const int64_t d = load_index<IdxT>(p.dev_idx, pair);
+    const int64_t h = p.paged_idx ? load_index<IdxT>(p.paged_idx, pair) : tok;
+    const bool ok = d >= 0 && d < g.dev_tokens && h >= 0 && h < g.paged_tokens;
+    if (!ok && lane == 0 && p.err) atomicOr(p.err, HICACHE_DEVERR_RANGE);
+    for (int r = lane; r < nr; r += 32) {
+      const char* layer_dev = p.seg[lo + (l0 + r) * g.seg_stride].dev;
+      const int64_t src = int64_t(reinterpret_cast<uintptr_t>(layer_dev) -
+                                  reinterpret_cast<uintptr_t>(sg.dev)) + d * g.row_bytes;
+      const int64_t dst = h * g.paged_page_stride + int64_t(l0 + r) * g.row_bytes;
+      offs[r] = ok ? make_longlong2(src, dst) : make_longlong2(-1, -1);
+    }
+    __syncwarp();
+    const uint32_t total = uint32_t(nr) * g.cpr;
+    if (g.vec == 16) copy_chunks<uint4, 16>(offs, sg.dev, sg.paged, g, 0, total, lane);
+    else copy_chunks<uint32_t, 4>(offs, sg.dev, sg.paged, g, 0, total, lane);
+    __syncwarp();  // the table is rewritten by the next task
+    return lo;
+  }
+  // A task is rows_per_task whole rows, or one part of a row longer than a task.
   int64_t row0;
   int nr;
   uint32_t chunk0, total;
@@ -170,7 +196,9 @@ __device__ __forceinline__ int copy_task(const CopyParams<MAXSEG>& p, int64_t ta
   return lo;
 }
 
-template <typename IdxT, int MAXSEG, bool SIGNAL>
+// LAYER_ROWS: the launch has a pool in the layer-row mode (an all-layer backup
+// into a token-major host pool); other launches compile without that branch.
+template <typename IdxT, int MAXSEG, bool SIGNAL, bool LAYER_ROWS>
 __global__ void __launch_bounds__(kThreadsPerCta)
     row_copy_kernel(const __grid_constant__ CopyParams<MAXSEG> p) {
   __shared__ longlong2 row_offs[kWarpsPerCta][kMaxRowsPerTask];
@@ -182,7 +210,7 @@ __global__ void __launch_bounds__(kThreadsPerCta)
     const int64_t warps_total = int64_t(gridDim.x) * kWarpsPerCta;
     for (int64_t task = int64_t(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5); task < ntasks;
          task += warps_total)
-      copy_task<IdxT, MAXSEG>(p, task, lane, offs);
+      copy_task<IdxT, MAXSEG, LAYER_ROWS>(p, task, lane, offs);
   } else {
     // Tasks are handed out in strict order from one counter, so every task of
     // layer l is taken before any task of layer l+1 and a layer can only wait
@@ -195,7 +223,7 @@ __global__ void __launch_bounds__(kThreadsPerCta)
     int64_t task = __shfl_sync(0xffffffffu, claim, 0);
     while (task < ntasks) {
       claim = lane == 0 ? atomicAdd(next, 1u) : 0u;
-      const int layer = copy_task<IdxT, MAXSEG>(p, task, lane, offs) / p.sig.segs_per_layer;
+      const int layer = copy_task<IdxT, MAXSEG, false>(p, task, lane, offs) / p.sig.segs_per_layer;
       if (layer != cur_layer) {
         if (pending != 0) flush_layer(p, cur_layer, pending, lane);
         cur_layer = layer;

@@ -48,10 +48,24 @@ hicache_status launch_segments(const CopyParams<MAXSEG>& prm, int32_t index_bits
   const int max_ctas = cfg.max_ctas > 0 ? cfg.max_ctas : device_sm_count() * per_sm;
   const int64_t want = (ntasks + kWarpsPerCta - 1) / kWarpsPerCta;
   const int grid = int(std::max<int64_t>(1, std::min<int64_t>(want, max_ctas)));
-  if (index_bits == 32)
-    row_copy_kernel<int32_t, MAXSEG, SIGNAL><<<grid, kThreadsPerCta, 0, stream>>>(prm);
-  else
-    row_copy_kernel<int64_t, MAXSEG, SIGNAL><<<grid, kThreadsPerCta, 0, stream>>>(prm);
+  bool layer_rows = false;
+  for (int p = 0; p < kMaxPools; ++p) layer_rows = layer_rows || prm.pool[p].layer_rows;
+  if constexpr (SIGNAL) {
+    if (index_bits == 32)
+      row_copy_kernel<int32_t, MAXSEG, true, false><<<grid, kThreadsPerCta, 0, stream>>>(prm);
+    else
+      row_copy_kernel<int64_t, MAXSEG, true, false><<<grid, kThreadsPerCta, 0, stream>>>(prm);
+  } else if (layer_rows) {
+    if (index_bits == 32)
+      row_copy_kernel<int32_t, MAXSEG, false, true><<<grid, kThreadsPerCta, 0, stream>>>(prm);
+    else
+      row_copy_kernel<int64_t, MAXSEG, false, true><<<grid, kThreadsPerCta, 0, stream>>>(prm);
+  } else {
+    if (index_bits == 32)
+      row_copy_kernel<int32_t, MAXSEG, false, false><<<grid, kThreadsPerCta, 0, stream>>>(prm);
+    else
+      row_copy_kernel<int64_t, MAXSEG, false, false><<<grid, kThreadsPerCta, 0, stream>>>(prm);
+  }
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "row copy kernel launch");
   count_launch();
@@ -153,6 +167,10 @@ void fill_geometry(const PoolInfo& pi, int64_t npairs, int vec, int64_t paged_pa
   g->tasks_per_seg = g->parts_per_row > 1
                          ? g->nrows * g->parts_per_row
                          : (g->nrows + g->rows_per_task - 1) / g->rows_per_task;
+  g->layer_rows = 0;
+  g->num_layers = 0;
+  g->seg_stride = 0;
+  g->tasks_per_token = 0;
 }
 
 hicache_status launch_rows(const std::vector<PoolInfo>& pools, const SideSpec& side,
@@ -173,10 +191,29 @@ hicache_status launch_rows(const std::vector<PoolInfo>& pools, const SideSpec& s
     prm.dir = dir;
     prm.pair_begin = pair_begin;
     int64_t tasks_per_layer = 0;
+    const bool one_launch = int64_t(layer_end - layer_begin) * segs_per_layer <= maxseg;
     for (size_t p = 0; p < pools.size(); ++p) {
-      fill_geometry(pools[p], npairs, side.vec16[p] ? 16 : 4, side.page_stride[p],
-                    side.paged_tokens[p], side.rows_per_page[p], &prm.pool[p]);
-      tasks_per_layer += int64_t(pools[p].T) * prm.pool[p].tasks_per_seg;
+      const PoolInfo& pi = pools[p];
+      PoolGeom& g = prm.pool[p];
+      fill_geometry(pi, npairs, side.vec16[p] ? 16 : 4, side.page_stride[p],
+                    side.paged_tokens[p], side.rows_per_page[p], &g);
+      // An all-layer backup into a token-major host pool whose rows do not fill
+      // whole lines: one task per token and up to kMaxRowsPerTask of its
+      // layers, which are adjacent on the host, instead of rows of one layer
+      // that each cover lines in part.
+      const int64_t R = pi.token_bytes;
+      if (dir == kDevToPaged && !signal && !cfg.paged_in_hbm && one_launch &&
+          layer_begin == 0 && layer_end == pi.L && !moves_page_rows(pi) &&
+          side.rows_per_page[p] == 1 && side.layer_stride[p] == R &&
+          side.page_stride[p] == int64_t(pi.L) * R && R <= kTaskBytes && R % 128 != 0) {
+        g.layer_rows = 1;
+        g.num_layers = pi.L;
+        g.seg_stride = segs_per_layer;
+        g.rows_per_task = std::min(pi.L, kMaxRowsPerTask);
+        g.tasks_per_token = (pi.L + g.rows_per_task - 1) / g.rows_per_task;
+        g.tasks_per_seg = g.nrows * g.tasks_per_token;  // all on the layer-0 segment
+      }
+      tasks_per_layer += int64_t(pi.T) * g.tasks_per_seg;
     }
     // A signalling launch covers whole layers only and counts its tasks in
     // 32-bit words; one layer must fit in one launch.
@@ -225,7 +262,8 @@ hicache_status launch_rows(const std::vector<PoolInfo>& pools, const SideSpec& s
           s.pool = int32_t(p);
           s.pad = 0;
           prm.seg_task_begin[nseg] = tasks;
-          tasks += prm.pool[p].tasks_per_seg;
+          // a layer-row pool's tasks all belong to its layer-0 segment
+          if (!prm.pool[p].layer_rows || l == layer_begin) tasks += prm.pool[p].tasks_per_seg;
           ++nseg;
         }
       }

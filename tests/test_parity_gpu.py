@@ -377,6 +377,79 @@ def test_page_first_layout_backup_then_load(where, path):
     G.assert_device_equal(pool, dev1, "page_first burst")
 
 
+# (L, T, head_num, head_dim, dtype_size): token-major pools whose rows do not fill
+# whole lines take one task per token over its adjacent host layers in the backup
+LAYER_ROW_CASES = [
+    (1, 1, 1, 66, 2),     # 132-byte rows, a single layer
+    (3, 2, 1, 18, 2),     # 36-byte rows
+    (78, 1, 1, 132, 1),   # the DSA indexer's token rows
+    (130, 1, 2, 36, 2),   # 144-byte rows, two tasks per token (128 + 2 layers)
+    (300, 2, 1, 2, 2),    # 4-byte rows; 600 segments: more than one launch holds
+]
+
+
+@pytest.mark.parametrize("case", LAYER_ROW_CASES, ids=[f"L{c[0]}_T{c[1]}_R{c[2]*c[3]*c[4]}"
+                                                       for c in LAYER_ROW_CASES])
+@pytest.mark.parametrize("where", ["device", "host"])
+@pytest.mark.parametrize("dtype", [torch.int32, torch.int64])
+@pytest.mark.parametrize("order", ["as_allocated", "falling_addresses"])
+def test_token_major_backup_by_layer_rows(case, where, dtype, order):
+    """falling_addresses: each tensor's layer buffers sorted so that layer 0 has the
+    highest address, which makes every layer's offset from layer 0 negative."""
+    import dataclasses
+
+    L, T, hn, hd, ds = case
+    s = G.shape(L=L, T=T, head_num=hn, head_dim=hd, dtype_size=ds, P=16, slots=1024, pages=48,
+                layout="page_first")
+    pool = G.make_pool(s, seed=50 + L)
+    if order == "falling_addresses":
+        pool = dataclasses.replace(pool, device_layers=[
+            sorted(per_t, key=lambda b: -b.data_ptr()) for per_t in pool.device_layers])
+        assert pool.device_layers[0][0].data_ptr() > pool.device_layers[0][-1].data_ptr() or L == 1
+    n = 16 * 20 - 5  # a partial last page
+    d, h = W.token_pairs(51 + L, n, s.device_slots, s.host_pages * 16, 16, fragmented=True)
+    d = d.copy()
+    d[7] = d[3]  # backup sources may repeat
+    dev0, host0 = G.device_images(pool), G.host_images(pool)
+    dt, ht = G.index_tensors(d, h, where, dtype)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    hk.hicache_backup_all_layers(pool, dt, ht, opts=_opts(hk.HICACHE_PATH_ZERO_COPY, where,
+                                                          device_error=err))
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    G.oracle_backup(pool, dev0, host0, d, h)
+    G.assert_host_equal(pool, host0, f"layer-row backup {case}")
+
+
+def test_layer_rows_beside_a_direct_pool_and_bad_device_pairs():
+    """An MLA latent pool (page_first_direct) and a token-major indexer pool in one
+    backup; bad device-located pairs are skipped and flagged in both."""
+    lat = G.shape("mla", L=6, T=1, head_num=1, head_dim=576, dtype_size=2, P=64,
+                  slots=64 * 32, pages=20)
+    idx = G.shape("dsa", L=6, T=1, head_num=1, head_dim=132, dtype_size=1, P=64,
+                  slots=64 * 32, pages=20, page_granular=True, value_kind="uint8_uniform",
+                  layout="page_first")
+    pools = [G.make_pool(lat, 52), G.make_pool(idx, 53)]
+    d, h, _, _ = W.page_pairs(54, 9, 32, 20, 64)
+    d, h = d.copy(), h.copy()
+    d[70] = 64 * 32 + 5  # out of range on the device side
+    h[200] = -3          # and on the host side
+    imgs = [(G.device_images(p), G.host_images(p)) for p in pools]
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dt, ht = G.index_tensors(d, h, "device")
+    hk.hicache_backup_all_layers(pools, dt, ht, opts=_opts(hk.HICACHE_PATH_ZERO_COPY, "device",
+                                                           device_error=err))
+    torch.cuda.synchronize()
+    assert int(err.item()) & hk.HICACHE_DEVERR_RANGE
+    keep = np.ones(d.size, dtype=bool)
+    keep[[70, 200]] = False
+    # both pools move token rows here, so exactly the two bad pairs are skipped
+    G.oracle_backup(pools[0], imgs[0][0], imgs[0][1], d[keep], h[keep])
+    G.assert_host_equal(pools[0], imgs[0][1], "latent pool")
+    G.oracle_backup(pools[1], imgs[1][0], imgs[1][1], d[keep], h[keep])
+    G.assert_host_equal(pools[1], imgs[1][1], "token-major indexer pool")
+
+
 # (layout, moved pages, staging in layer blocks of every moved page, layer range).
 # Group sizes grow 1, 2, 4, ... while a staging buffer holds every page of the
 # group, or chunks of at least 32 pages of it.
