@@ -55,20 +55,24 @@ __device__ __forceinline__ void flush_layer(const CopyParams<MAXSEG>& p, int lay
 // destination byte offsets of task row r (y < 0 marks a skipped row: a
 // destination offset is never negative, a source offset may be); (r, j)
 // is the (row, chunk-in-row) position of chunk chunk0 + c0 + lane and advances
-// by precomputed quotients, so the loop has no division.
-template <typename V, int VEC>
+// by precomputed quotients, so the loop has no division.  Each lane keeps
+// UNROLL chunks in flight.
+template <typename V, int VEC, int UNROLL = kUnroll>
 __device__ __forceinline__ void copy_chunks(const longlong2* offs, const char* src, char* dst,
                                             const PoolGeom& g, uint32_t chunk0, uint32_t total,
                                             int lane) {
   const uint32_t cpr = g.cpr;
+  // advance of 32 * UNROLL chunks as whole rows and a remainder
+  const uint32_t qS = UNROLL == kUnroll ? g.qS : uint32_t(32 * UNROLL) / cpr;
+  const uint32_t rS = UNROLL == kUnroll ? g.rS : uint32_t(32 * UNROLL) - qS * cpr;
   uint32_t r = (chunk0 + uint32_t(lane)) / cpr;
   uint32_t j = (chunk0 + uint32_t(lane)) - r * cpr;
-  for (uint32_t c0 = 0; c0 < total; c0 += 32u * kUnroll) {
-    V v[kUnroll];
-    int64_t dpos[kUnroll];
+  for (uint32_t c0 = 0; c0 < total; c0 += 32u * UNROLL) {
+    V v[UNROLL];
+    int64_t dpos[UNROLL];
     uint32_t rr = r, jj = j;
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
+    for (int u = 0; u < UNROLL; ++u) {
       dpos[u] = -1;
       if (c0 + uint32_t(lane) + 32u * u < total) {
         const longlong2 o = offs[rr];
@@ -83,11 +87,11 @@ __device__ __forceinline__ void copy_chunks(const longlong2* offs, const char* s
       if (jj >= cpr) { jj -= cpr; ++rr; }
     }
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u)
+    for (int u = 0; u < UNROLL; ++u)
       if (dpos[u] >= 0) st_stream(reinterpret_cast<V*>(dst + dpos[u]), v[u]);
-    // advance by 32 * kUnroll chunks
-    j += g.rS;
-    r += g.qS;
+    // advance by 32 * UNROLL chunks
+    j += rS;
+    r += qS;
     if (j >= cpr) { j -= cpr; ++r; }
   }
 }
@@ -127,8 +131,10 @@ __device__ __forceinline__ int copy_task(const CopyParams<MAXSEG>& p, int64_t ta
     }
     __syncwarp();
     const uint32_t total = uint32_t(nr) * g.cpr;
+    // 4-byte chunks keep four times as many in flight, so that a lane has as
+    // many bytes outstanding on the host link as with 16-byte chunks
     if (g.vec == 16) copy_chunks<uint4, 16>(offs, sg.dev, sg.paged, g, 0, total, lane);
-    else copy_chunks<uint32_t, 4>(offs, sg.dev, sg.paged, g, 0, total, lane);
+    else copy_chunks<uint32_t, 4, 4 * kUnroll>(offs, sg.dev, sg.paged, g, 0, total, lane);
     __syncwarp();  // the table is rewritten by the next task
     return lo;
   }
