@@ -12,6 +12,7 @@ import glob
 import os
 import shutil
 import subprocess
+import time
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 REPO = os.path.dirname(HERE)
@@ -57,10 +58,28 @@ def up_to_date() -> bool:
 
 
 def build(force: bool = False, ptxas_verbose: bool = False, quiet: bool = True) -> str:
-    """Compile and link the library; returns its path."""
+    """Compile and link the library; returns its path.
+
+    Processes that build at the same time (the ranks of a multi-GPU run, parallel
+    test workers) take turns on a lock file, and a process that finds the library
+    current once it holds the lock does not rebuild it.
+    """
+    import fcntl
+
     if not force and not ptxas_verbose and up_to_date():
         return LIB_PATH
     os.makedirs(BUILD_DIR, exist_ok=True)
+    asked = time.time()
+    with open(os.path.join(BUILD_DIR, ".lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)  # released when the file closes
+        # another process may have built it while this one waited
+        if (not ptxas_verbose and up_to_date()
+                and (not force or os.path.getmtime(LIB_PATH) >= asked)):
+            return LIB_PATH
+        return _build_locked(ptxas_verbose, quiet)
+
+
+def _build_locked(ptxas_verbose: bool, quiet: bool) -> str:
     jobs = []
     for src in _sources():
         obj = os.path.join(BUILD_DIR, os.path.basename(src) + ".o")

@@ -225,3 +225,25 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(B, "LIB_PATH", str(tmp_path / "absent.so"))
     with pytest.raises(RuntimeError, match="missing"):
         B.lib()
+
+
+def test_concurrent_builds_compile_once(tmp_path):
+    """Processes that build at the same time (ranks of a multi-GPU run) take turns
+    on a lock: one compiles, the others find the library current and load it."""
+    import subprocess
+    import sys
+
+    code = ("import time, hierarchical_kv_cache_gb300.build as b; t = time.time(); "
+            "b.build(force=True); print(round(time.time() - t, 2))")
+    procs = [subprocess.Popen([sys.executable, "-c", code], cwd=REPO, stdout=subprocess.PIPE,
+                              stderr=subprocess.PIPE, text=True) for _ in range(3)]
+    outs = [p.communicate(timeout=600) for p in procs]
+    assert all(p.returncode == 0 for p in procs), [o[1][-2000:] for o in outs]
+    mtime = os.path.getmtime(B.LIB_PATH)
+    # one build: the library is newer than every object file the others could have written
+    objs = [os.path.join(os.path.dirname(B.LIB_PATH), "_build", f)
+            for f in os.listdir(os.path.join(os.path.dirname(B.LIB_PATH), "_build"))
+            if f.endswith(".o")]
+    assert objs and all(os.path.getmtime(o) <= mtime for o in objs)
+    lib = ctypes.CDLL(B.LIB_PATH)
+    assert lib.hicache_abi_version() == 4
