@@ -106,10 +106,15 @@ hicache_status signaled_burst(const std::vector<PoolInfo>& pools, const SideSpec
   }
   const LaunchCfg cfg{o.max_ctas, o.device_error};
   // The first layer is latency-critical (nothing downstream can start before
-  // it), so it gets a launch of its own and its event on the caller's stream;
-  // the remaining layers share one signalling launch.
+  // it), so a large one gets a launch of its own and its event on the caller's
+  // stream; the remaining layers share one signalling launch.  A small burst
+  // runs as one signalling launch: there a second launch costs more than the
+  // first layer gains from the link to itself.
+  int64_t layer_bytes = 0;
+  for (const PoolInfo& pi : pools)
+    layer_bytes += int64_t(pi.T) * moved_row_bytes(pi) * (moves_page_rows(pi) ? idx.n / pi.P : idx.n);
   int32_t first = 0;  // burst-relative index of the first signalled layer
-  if (count >= 2) {
+  if (count >= 2 && layer_bytes >= kSplitFirstLayerBytes) {
     st = launch_rows(pools, side, idx.dev_gpu, idx.host_gpu, idx.bits, 0, idx.n, kPagedToDev,
                      layer_begin, layer_begin + 1, cfg, stream);
     cudaError_t e0 = cudaSuccess;
