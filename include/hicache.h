@@ -203,10 +203,11 @@ hicache_status hicache_load_layer(const hicache_pool* pools, int32_t num_pools, 
  * Without opts->burst_words, each layer is one kernel launch on `stream`
  * followed by cudaEventRecord(layer_done[...], stream).  With
  * opts->burst_words (device memory, at least 4 * (layer_end - layer_begin)
- * words, zeroed by the call itself), a zero-copy burst takes two launches: the
- * first layer alone (its event recorded on `stream`), then one launch covering
- * all other layers, its tasks handed out in layer order: the kernel sets one
- * word per layer as the layer completes, a
+ * words, zeroed by the call itself), a zero-copy burst takes two launches when
+ * a layer holds 16 MiB or more: the first layer alone (its event recorded on
+ * `stream`), then one launch covering all other layers; a smaller burst is
+ * that one launch alone.  Its tasks are handed out in layer order: the kernel
+ * sets one word per layer as the layer completes, a
  * library stream forked from `stream` waits on each word with a stream memory
  * wait and records the layer's event, and `stream` joins that stream before
  * the call returns.  The words must not be shared by bursts that overlap on the
