@@ -57,10 +57,13 @@ struct PoolGeom {
   // the host, so that its host writes cover whole lines.  Its rows are layers;
   // every task of the (pool, tensor) belongs to its layer-0 segment, and layer
   // l's device buffer is the one of segment (that segment + l * seg_stride).
+  // A token whose layers hold little (L * R well under a task) shares a task
+  // with the next tokens: row f of such a task is layer f % L of its token f / L.
   int32_t layer_rows;        // 1 = this mode
   int32_t num_layers;        // L (layer rows only)
   int32_t seg_stride;        // segments from one layer to the next (layer rows only)
-  int32_t tasks_per_token;   // ceil(L / rows_per_task) (layer rows only)
+  int32_t tasks_per_token;   // ceil(L / rows_per_task) when a token spans tasks, else 1
+  int32_t tokens_per_task;   // tokens sharing a task (1 when a token spans tasks)
 };
 
 // One (pool, tensor, layer) stream.

@@ -112,23 +112,44 @@ __device__ __forceinline__ int copy_task(const CopyParams<MAXSEG>& p, int64_t ta
   const PoolGeom& g = p.pool[sg.pool];
   const int64_t t = task - p.seg_task_begin[lo];
   if (LAYER_ROWS && g.layer_rows) {
-    // Layers [l0, l0 + nr) of one token: row r is layer l0 + r, read from that
-    // layer's own segment and written to the token's adjacent host rows.
-    const int64_t tok = t / g.tasks_per_token;
-    const int l0 = int(t - tok * g.tasks_per_token) * g.rows_per_task;
-    const int nr = min(g.rows_per_task, g.num_layers - l0);
-    const int64_t pair = p.pair_begin + tok;
-    const int64_t d = load_index<IdxT>(p.dev_idx, pair);
-    const int64_t h = p.paged_idx ? load_index<IdxT>(p.paged_idx, pair) : tok;
-    const bool ok = d >= 0 && d < g.dev_tokens && h >= 0 && h < g.paged_tokens;
-    if (!ok && lane == 0 && p.err) atomicOr(p.err, HICACHE_DEVERR_RANGE);
-    for (int r = lane; r < nr; r += 32) {
-      const char* layer_dev = p.seg[lo + (l0 + r) * g.seg_stride].dev;
+    // Rows [l0, l0 + nr) of the (token, layer) order of the task's tokens,
+    // which start at tok0: row f is layer f % L of token tok0 + f / L, read
+    // from that layer's own segment and written next to the token's other
+    // layers on the host.  l0 is 0 unless one token spans several tasks.
+    const int L = g.num_layers;
+    const int64_t tok0 = (t / g.tasks_per_token) * g.tokens_per_task;
+    const int l0 = int(t % g.tasks_per_token) * g.rows_per_task;
+    const int nr = g.tasks_per_token > 1
+                       ? min(g.rows_per_task, L - l0)
+                       : int(min(int64_t(g.tokens_per_task), g.nrows - tok0)) * L;
+    constexpr int kRowsPerLane = kMaxRowsPerTask / 32;
+    int64_t dv[kRowsPerLane], hv[kRowsPerLane];
+#pragma unroll
+    for (int q = 0; q < kRowsPerLane; ++q) {  // every index load first
+      const int r = lane + 32 * q;
+      if (r < nr) {
+        const int64_t tok = tok0 + (l0 + r) / L;
+        dv[q] = load_index<IdxT>(p.dev_idx, p.pair_begin + tok);
+        hv[q] = p.paged_idx ? load_index<IdxT>(p.paged_idx, p.pair_begin + tok) : tok;
+      }
+    }
+    bool bad = false;
+#pragma unroll
+    for (int q = 0; q < kRowsPerLane; ++q) {
+      const int r = lane + 32 * q;
+      if (r >= nr) break;
+      const int f = l0 + r;
+      const int l = f - (f / L) * L;
+      const int64_t d = dv[q], h = hv[q];
+      const bool ok = d >= 0 && d < g.dev_tokens && h >= 0 && h < g.paged_tokens;
+      bad = bad || !ok;
+      const char* layer_dev = p.seg[lo + l * g.seg_stride].dev;
       const int64_t src = int64_t(reinterpret_cast<uintptr_t>(layer_dev) -
                                   reinterpret_cast<uintptr_t>(sg.dev)) + d * g.row_bytes;
-      const int64_t dst = h * g.paged_page_stride + int64_t(l0 + r) * g.row_bytes;
+      const int64_t dst = h * g.paged_page_stride + int64_t(l) * g.row_bytes;
       offs[r] = ok ? make_longlong2(src, dst) : make_longlong2(-1, -1);
     }
+    if (__any_sync(0xffffffffu, bad) && lane == 0 && p.err) atomicOr(p.err, HICACHE_DEVERR_RANGE);
     __syncwarp();
     const uint32_t total = uint32_t(nr) * g.cpr;
     // 4-byte chunks keep four times as many in flight, so that a lane has as

@@ -171,6 +171,7 @@ void fill_geometry(const PoolInfo& pi, int64_t npairs, int vec, int64_t paged_pa
   g->num_layers = 0;
   g->seg_stride = 0;
   g->tasks_per_token = 0;
+  g->tokens_per_task = 0;
 }
 
 hicache_status launch_rows(const std::vector<PoolInfo>& pools, const SideSpec& side,
@@ -209,9 +210,17 @@ hicache_status launch_rows(const std::vector<PoolInfo>& pools, const SideSpec& s
         g.layer_rows = 1;
         g.num_layers = pi.L;
         g.seg_stride = segs_per_layer;
-        g.rows_per_task = std::min(pi.L, kMaxRowsPerTask);
-        g.tasks_per_token = (pi.L + g.rows_per_task - 1) / g.rows_per_task;
-        g.tasks_per_seg = g.nrows * g.tasks_per_token;  // all on the layer-0 segment
+        // about kTaskBytes of adjacent host rows per task: several tokens when
+        // a token's layers hold less, part of a token when it has more than
+        // kMaxRowsPerTask layers
+        const int64_t per_token = int64_t(pi.L) * R;
+        const int64_t kt = std::min<int64_t>(std::max<int64_t>(1, (kTaskBytes + per_token - 1) / per_token),
+                                             std::max<int64_t>(1, kMaxRowsPerTask / pi.L));
+        g.tokens_per_task = int32_t(kt);
+        g.rows_per_task = pi.L >= kMaxRowsPerTask ? kMaxRowsPerTask : int32_t(kt) * pi.L;
+        g.tasks_per_token = (pi.L + g.rows_per_task - 1) / g.rows_per_task;  // 1 unless L > 128
+        g.tasks_per_seg = g.tasks_per_token > 1 ? g.nrows * g.tasks_per_token
+                                                : (g.nrows + kt - 1) / kt;  // all on layer 0's segment
       }
       tasks_per_layer += int64_t(pi.T) * g.tasks_per_seg;
     }
