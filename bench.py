@@ -23,6 +23,7 @@ of the same workload, the only baseline that exists for this path.
 from __future__ import annotations
 
 import argparse
+import contextlib
 import json
 import os
 import statistics
@@ -304,6 +305,59 @@ def traffic_per_launch(which, algorithmic_bytes):
     return int(per_byte * algorithmic_bytes)
 
 
+# ---------------------------------------------------------------- host placement
+
+def _read(path):
+    try:
+        with open(path) as f:
+            return f.read().strip()
+    except OSError:
+        return None
+
+
+def _cpulist(text):
+    """'0-3,8' -> {0, 1, 2, 3, 8}."""
+    cpus = set()
+    for part in (text or "").split(","):
+        if "-" in part:
+            a, b = part.split("-")
+            cpus.update(range(int(a), int(b) + 1))
+        elif part.strip():
+            cpus.add(int(part))
+    return cpus
+
+
+@contextlib.contextmanager
+def pinned_allocation_near_gpu(dev):
+    """Binds the process to the GPU's local CPUs while the pinned pools are first
+    touched, so that their pages land on the NUMA node attached to the GPU, and
+    restores the previous affinity afterwards (the CPU baseline keeps every core).
+    Yields what the system reports: the GPU's PCI address, NUMA node and local
+    CPUs, the nodes online, and whether the affinity had to change."""
+    import torch
+    info = {"nodes_online": _read("/sys/devices/system/node/online")}
+    prop = torch.cuda.get_device_properties(dev)
+    try:
+        addr = "%04x:%02x:%02x.0" % (prop.pci_domain_id, prop.pci_bus_id, prop.pci_device_id)
+    except AttributeError:
+        addr = None
+    if addr:
+        base = f"/sys/bus/pci/devices/{addr}"
+        info.update(pci=addr, gpu_numa_node=_read(base + "/numa_node"),
+                    gpu_local_cpus=_read(base + "/local_cpulist"))
+    old = os.sched_getaffinity(0)
+    near = _cpulist(info.get("gpu_local_cpus")) & old
+    bound = bool(near) and near != old
+    info["bound_for_allocation"] = bound
+    if bound:
+        os.sched_setaffinity(0, near)
+    try:
+        yield info
+    finally:
+        if bound:
+            os.sched_setaffinity(0, old)
+
+
 # ---------------------------------------------------------------- workload
 
 def build_workload(name, seed_offset=0, args=None):
@@ -351,13 +405,14 @@ def run_ours(args, rank, world):
     n = d.size
     t_alloc = time.time()
     pools = []
-    for i, s in enumerate(wl.pools):
-        p = hpools.allocate_pool(s)
-        hpools.fill_device_random_(p, wl.seed + i, s.value_kind)
-        for ht in p.host_tensors:
-            ht.zero_()
-        pools.append(p)
-    torch.cuda.synchronize()
+    with pinned_allocation_near_gpu(torch.cuda.current_device()) as placement:
+        for i, s in enumerate(wl.pools):
+            p = hpools.allocate_pool(s)
+            hpools.fill_device_random_(p, wl.seed + i, s.value_kind)
+            for ht in p.host_tensors:
+                ht.zero_()
+            pools.append(p)
+        torch.cuda.synchronize()
     t_alloc = time.time() - t_alloc
 
     path = {"auto": hk.HICACHE_PATH_AUTO, "zero_copy": hk.HICACHE_PATH_ZERO_COPY,
@@ -495,6 +550,7 @@ def run_ours(args, rank, world):
             "l2": "inputs larger than L2 (pools of GiBs on each side), no flush",
             "parallelism": f"replicas x{world}",
             "host_alloc_s": round(t_alloc, 1),
+            "host_placement": placement,
         },
         "ops": {
             "backup_d2h_gbs": round(backup_gbs, 2),

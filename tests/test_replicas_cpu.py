@@ -59,3 +59,11 @@ def test_single_rank_needs_no_process_group():
 
     assert bench.max_over_ranks(3.5, 1) == 3.5
     assert abs(bench.aggregate_gbs(1, 2, 1e9, 1000.0) - 2.0) < 1e-12
+
+
+def test_cpu_list_parsing_for_host_placement():
+    """The bench binds pool allocation to the CPUs sysfs lists as local to the GPU."""
+    import bench
+    assert bench._cpulist("0-3,8,10-11") == {0, 1, 2, 3, 8, 10, 11}
+    assert bench._cpulist("") == set() and bench._cpulist(None) == set()
+    assert bench._cpulist("5") == {5}
