@@ -6,8 +6,8 @@
 // the host.  Here the staging is double-buffered so that the gather of chunk
 // k+1 overlaps the link transfer of chunk k, the DMA is one copy per run of
 // consecutive host pages (not one per row), and the same idea serves the
-// per-layer load in reverse (2-D DMA of one layer block per host page, then a
-// scatter kernel).  The staged path needs the pairs to be whole host pages in
+// per-layer load in reverse (2-D DMA of a group of layer blocks per host page,
+// then a scatter kernel per layer; a burst's first layer is read zero-copy).  The staged path needs the pairs to be whole host pages in
 // groups of page_size (what a page-granular host allocator hands out) and the
 // indices on the host, because the DMA spans are planned on the CPU.
 #include <cuda_runtime.h>
@@ -252,9 +252,24 @@ hicache_status staged_load(const std::vector<PoolInfo>& pools, const hicache_opt
 
   HK_TRY(cudaEventRecord(r->fork, stream), "cudaEventRecord(fork)");
   HK_TRY(cudaStreamWaitEvent(copy, r->fork, 0), "cudaStreamWaitEvent(fork)");
+  int32_t first = layer_begin;
+  if (count >= 2) {
+    // The first layer of a burst is latency-critical, and through the copy
+    // engine it would cost one small copy per host page before its event.  It
+    // is read zero-copy instead (the SMs read the host pool directly), while
+    // the copy stream already moves the next group.
+    const LaunchCfg direct{o.max_ctas, o.device_error, /*paged_in_hbm=*/false};
+    st = launch_rows(pools, host_side(pools), idx.dev_gpu, idx.host_gpu, idx.bits, 0, idx.n,
+                     kPagedToDev, layer_begin, layer_begin + 1, direct, stream);
+    if (st != HICACHE_OK) return finish(st);
+    if (layer_done && layer_done[0])
+      HK_TRY(cudaEventRecord(layer_done[0], stream), "cudaEventRecord(layer_done)");
+    recorded = 1;
+    first = layer_begin + 1;
+  }
   int64_t step = 0;
-  int32_t g_want = 1;
-  for (int32_t l = layer_begin, g = 1; l < layer_end; l += g) {
+  int32_t g_want = first == layer_begin ? 1 : 2;
+  for (int32_t l = first, g = 1; l < layer_end; l += g) {
     // the next group size; a tail shorter than the group joins it rather
     // than paying for small copies of its own
     g = std::min(g_want, layer_end - l);

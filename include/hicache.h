@@ -212,11 +212,13 @@ hicache_status hicache_load_layer(const hicache_pool* pools, int32_t num_pools, 
  * wait and records the layer's event, and `stream` joins that stream before
  * the call returns.  The words must not be shared by bursts that overlap on the
  * GPU.  The staged path ignores burst_words.
- * The staged path copies groups of consecutive layers of each host page per
- * DMA, groups of 1, 2, 4, ... layers (up to about 4 MiB per copy, in chunks
- * of pages that fit a staging buffer), then scatters and records the events
- * of a group's layers one by one.  Its layer events therefore arrive in
- * groups, each no earlier than its own layer's data.
+ * The staged path reads the first layer of a burst of two or more layers
+ * zero-copy (the SMs read the host pool), then copies groups of consecutive
+ * layers of each host page per DMA, groups of 2, 4, ... layers (up to about
+ * 4 MiB per copy, in chunks of pages that fit a staging buffer), and scatters
+ * and records the events of a group's layers one by one.  Its later layer
+ * events therefore arrive in groups, each no earlier than its own layer's
+ * data.
  */
 hicache_status hicache_load_burst(const hicache_pool* pools, int32_t num_pools,
                                   int32_t layer_begin, int32_t layer_end,
