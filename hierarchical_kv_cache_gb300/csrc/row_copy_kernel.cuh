@@ -99,7 +99,7 @@ __device__ __forceinline__ void copy_chunks(const longlong2* offs, const char* s
 // Copies the rows of one warp task and returns the task's launch-relative
 // segment.  Called by all 32 lanes of a warp; offs is the warp's table of
 // kMaxRowsPerTask entries in shared memory.
-template <typename IdxT, int MAXSEG, bool LAYER_ROWS>
+template <typename IdxT, int MAXSEG, bool LAYER_ROWS, bool DEEP4>
 __device__ __forceinline__ int copy_task(const CopyParams<MAXSEG>& p, int64_t task, int lane,
                                          longlong2* offs) {
   // segment of this task: last s with seg_task_begin[s] <= task
@@ -218,14 +218,17 @@ __device__ __forceinline__ int copy_task(const CopyParams<MAXSEG>& p, int64_t ta
   const char* src = p.dir == kDevToPaged ? sg.dev : sg.paged;
   char* dst = p.dir == kDevToPaged ? sg.paged : sg.dev;
   if (g.vec == 16) copy_chunks<uint4, 16>(offs, src, dst, g, chunk0, total, lane);
-  else copy_chunks<uint32_t, 4>(offs, src, dst, g, chunk0, total, lane);
+  else copy_chunks<uint32_t, 4, DEEP4 ? 4 * kUnroll : kUnroll>(offs, src, dst, g, chunk0, total, lane);
   __syncwarp();  // the table is rewritten by the next task
   return lo;
 }
 
 // LAYER_ROWS: the launch has a pool in the layer-row mode (an all-layer backup
 // into a token-major host pool); other launches compile without that branch.
-template <typename IdxT, int MAXSEG, bool SIGNAL, bool LAYER_ROWS>
+// DEEP4: the launch has a pool that takes 4-byte chunks; they run four times
+// as deep, so that a lane keeps as many bytes in flight as with 16-byte
+// chunks.  Launches of 16-byte chunks only compile with the shallow loop.
+template <typename IdxT, int MAXSEG, bool SIGNAL, bool LAYER_ROWS, bool DEEP4>
 __global__ void __launch_bounds__(kThreadsPerCta)
     row_copy_kernel(const __grid_constant__ CopyParams<MAXSEG> p) {
   __shared__ longlong2 row_offs[kWarpsPerCta][kMaxRowsPerTask];
@@ -237,7 +240,7 @@ __global__ void __launch_bounds__(kThreadsPerCta)
     const int64_t warps_total = int64_t(gridDim.x) * kWarpsPerCta;
     for (int64_t task = int64_t(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5); task < ntasks;
          task += warps_total)
-      copy_task<IdxT, MAXSEG, LAYER_ROWS>(p, task, lane, offs);
+      copy_task<IdxT, MAXSEG, LAYER_ROWS, DEEP4>(p, task, lane, offs);
   } else {
     // Tasks are handed out in strict order from one counter, so every task of
     // layer l is taken before any task of layer l+1 and a layer can only wait
@@ -250,7 +253,7 @@ __global__ void __launch_bounds__(kThreadsPerCta)
     int64_t task = __shfl_sync(0xffffffffu, claim, 0);
     while (task < ntasks) {
       claim = lane == 0 ? atomicAdd(next, 1u) : 0u;
-      const int layer = copy_task<IdxT, MAXSEG, false>(p, task, lane, offs) / p.sig.segs_per_layer;
+      const int layer = copy_task<IdxT, MAXSEG, false, DEEP4>(p, task, lane, offs) / p.sig.segs_per_layer;
       if (layer != cur_layer) {
         if (pending != 0) flush_layer(p, cur_layer, pending, lane);
         cur_layer = layer;

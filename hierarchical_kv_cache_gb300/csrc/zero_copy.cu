@@ -48,24 +48,32 @@ hicache_status launch_segments(const CopyParams<MAXSEG>& prm, int32_t index_bits
   const int max_ctas = cfg.max_ctas > 0 ? cfg.max_ctas : device_sm_count() * per_sm;
   const int64_t want = (ntasks + kWarpsPerCta - 1) / kWarpsPerCta;
   const int grid = int(std::max<int64_t>(1, std::min<int64_t>(want, max_ctas)));
-  bool layer_rows = false;
-  for (int p = 0; p < kMaxPools; ++p) layer_rows = layer_rows || prm.pool[p].layer_rows;
-  if constexpr (SIGNAL) {
-    if (index_bits == 32)
-      row_copy_kernel<int32_t, MAXSEG, true, false><<<grid, kThreadsPerCta, 0, stream>>>(prm);
-    else
-      row_copy_kernel<int64_t, MAXSEG, true, false><<<grid, kThreadsPerCta, 0, stream>>>(prm);
-  } else if (layer_rows) {
-    if (index_bits == 32)
-      row_copy_kernel<int32_t, MAXSEG, false, true><<<grid, kThreadsPerCta, 0, stream>>>(prm);
-    else
-      row_copy_kernel<int64_t, MAXSEG, false, true><<<grid, kThreadsPerCta, 0, stream>>>(prm);
-  } else {
-    if (index_bits == 32)
-      row_copy_kernel<int32_t, MAXSEG, false, false><<<grid, kThreadsPerCta, 0, stream>>>(prm);
-    else
-      row_copy_kernel<int64_t, MAXSEG, false, false><<<grid, kThreadsPerCta, 0, stream>>>(prm);
+  bool layer_rows = false, deep4 = false;
+  for (int p = 0; p < kMaxPools; ++p) {
+    layer_rows = layer_rows || prm.pool[p].layer_rows;
+    deep4 = deep4 || prm.pool[p].vec == 4;
   }
+  // one instance per index width, signalling, layer rows and 4-byte chunks
+  auto go = [&](auto idx_tag, auto lr_tag, auto d4_tag) {
+    using IdxT = decltype(idx_tag);
+    row_copy_kernel<IdxT, MAXSEG, SIGNAL, decltype(lr_tag)::value, decltype(d4_tag)::value>
+        <<<grid, kThreadsPerCta, 0, stream>>>(prm);
+  };
+  using F = std::false_type;
+  using T = std::true_type;
+  auto pick = [&](auto idx_tag) {
+    if constexpr (SIGNAL) {
+      if (deep4) go(idx_tag, F{}, T{}); else go(idx_tag, F{}, F{});
+    } else if (layer_rows) {
+      // the layer-row path runs 4-byte chunks deep by itself; the other pools
+      // of such a launch take the shallow loop (a deep one measured slower)
+      go(idx_tag, T{}, F{});
+    } else {
+      if (deep4) go(idx_tag, F{}, T{}); else go(idx_tag, F{}, F{});
+    }
+  };
+  if (index_bits == 32) pick(int32_t{});
+  else pick(int64_t{});
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "row copy kernel launch");
   count_launch();
