@@ -14,6 +14,7 @@ with:
 - no byte outside the named rows changes (counted, not located by formula);
 - pair order does not matter; an empty pair list changes nothing;
 - the page counts 1/63/64/65/128/129 that the pages' unit test probes;
+- brute force over a tiny pool: every (device slot, host slot) pair alone;
 - structural facts of page-first storage read off tagged rows: one host page is
   one contiguous block holding exactly its own tokens for every layer, layer
   blocks in increasing layer order, tokens in increasing in-page order;
@@ -99,6 +100,35 @@ def pin_numpy_shape(lib):
             want_l = dev[l].copy().reshape(S, R)
             want_l[dd] = host4[hh // P, l, hh % P, :]
             assert np.array_equal(got_l, want_l.reshape(-1)), f"load vs numpy shape {(L, P, R, l)}"
+
+
+def pin_exhaustive_single_pairs(lib):
+    """Brute force over a tiny pool: every (device slot, host slot) pair alone.
+
+    For each pair the backup must change exactly the R bytes of every layer at
+    the [page][layer][token][row] position of that host slot, and the load of
+    each layer exactly the device row of that slot; found by comparing whole
+    images, not by an address formula.
+    """
+    L, P, R, S, H = 2, 2, 4, 8, 4
+    g = np.random.default_rng(17)
+    dev, host = _pool(g, L, P, R, S, H)
+    for d in range(S):
+        for h in range(H * P):
+            got = host.copy()
+            oracle.backup_all_layers(dev, got, np.array([d]), np.array([h]), page_size=P,
+                                     row_bytes=R, lib=lib)
+            want = host.copy().reshape(H, L, P, R)
+            for l in range(L):
+                want[h // P, l, h % P, :] = dev[l].reshape(S, R)[d]
+            assert np.array_equal(got, want.reshape(-1)), f"backup of the single pair {(d, h)}"
+            for l in range(L):
+                got_l = dev[l].copy()
+                oracle.load_layer(got_l, host, l, np.array([h]), np.array([d]), num_layers=L,
+                                  page_size=P, row_bytes=R, lib=lib)
+                want_l = dev[l].copy().reshape(S, R)
+                want_l[d] = host.reshape(H, L, P, R)[h // P, l, h % P]
+                assert np.array_equal(got_l, want_l.reshape(-1)), f"load of {(h, d)}, layer {l}"
 
 
 def pin_round_trip(lib):
@@ -317,6 +347,7 @@ PINS = [
     pin_golden_backup,
     pin_golden_load,
     pin_numpy_shape,
+    pin_exhaustive_single_pairs,
     pin_round_trip,
     pin_untouched,
     pin_permutation_and_empty,
