@@ -43,3 +43,15 @@ def test_reference_arm_other_ranks_print_nothing():
                   env={"RANK": "1", "WORLD_SIZE": "2"})
     assert r.returncode == 0, r.stderr[-2000:]
     assert not [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+
+
+def test_traffic_record_matches_the_kernel_source():
+    """bench.py reports DRAM traffic from a committed ncu record only while the
+    record's hash matches the kernel source; a kernel edit must re-take it."""
+    sys.path.insert(0, REPO)
+    import bench
+
+    for which in ("backup_all_layers", "load_one_layer", "load_burst_signalling"):
+        t = bench.traffic_per_launch(which, 1 << 30)
+        assert t is not None, f"{which}: the record does not match csrc/row_copy_kernel.cuh"
+        assert (1 << 30) * 0.95 < t < (1 << 30) * 1.05 or which != "backup_all_layers"
