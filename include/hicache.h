@@ -100,7 +100,10 @@ typedef enum hicache_index_location {
    * them completely before enqueueing (range, duplicate destinations, whole
    * pages) and the GPU reads them through their mapping (or from
    * opts->index_staging).  Device memory passed here is rejected with
-   * HICACHE_EINVAL before the CPU reads it. */
+   * HICACHE_EINVAL before the CPU reads it.  The check of distinct
+   * destinations keeps a bitmap of one bit per destination row on each calling
+   * thread, reused by later calls (for a destination space above 2^28 rows that
+   * a list uses sparsely, a sorted copy of the list instead). */
   HICACHE_INDEX_HOST = 0,
   /* Both index arrays are in device memory and may still be being written on
    * `stream`.  The CPU does not read them: kernels skip pairs that are out of
