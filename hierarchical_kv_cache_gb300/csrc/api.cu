@@ -310,6 +310,13 @@ extern "C" hicache_status hicache_load_burst(const hicache_pool* pools, int32_t 
 // array's name as a device address (in host code it names a host-side
 // stand-in); the device address is resolved once per device with
 // cudaGetSymbolAddress and handed to the staged backup as its two buffers.
+//
+// Everything that could place memory on the device is done by the set-up that
+// opens every call, a call with no pairs included: resolving the address loads
+// the module that holds the array (under CUDA's default lazy loading that is
+// when the array is placed in HBM), the copy kernels the staged backup launches
+// are loaded, and the calling thread's copy stream and events are created.
+// After one such call on a device and thread, later calls take no device memory.
 
 static __device__ __align__(256) unsigned char g_static_staging[HICACHE_STATIC_STAGING_BYTES];
 
@@ -319,22 +326,30 @@ namespace {
 std::mutex g_static_mu;
 void* g_static_addr[64] = {};
 
-// Device address of g_static_staging on the current device (resolved once).
-hicache_status static_staging_address(void** out) {
+// Device address of g_static_staging on the current device, resolved (and the
+// staged backup's kernels loaded) once per device.  A cudaDeviceReset destroys
+// the module and with it the cached address, so the entry point must not be
+// used on a device after it was reset.
+hicache_status static_staging_setup(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   if (dev < 0 || dev >= 64) return fail(HICACHE_EINVAL, "device ordinal above 63");
-  std::lock_guard<std::mutex> lock(g_static_mu);
-  if (!g_static_addr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_static_staging);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static staging array)");
-    if (!p) return fail(HICACHE_ECUDA, "cudaGetSymbolAddress returned NULL for the staging array");
-    g_static_addr[dev] = p;
+  {
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (!g_static_addr[dev]) {
+      void* p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_static_staging);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static staging array)");
+      if (!p) return fail(HICACHE_ECUDA, "cudaGetSymbolAddress returned NULL for the staging array");
+      const hicache_status st = load_staged_backup_kernels();
+      if (st != HICACHE_OK) return st;
+      g_static_addr[dev] = p;
+    }
+    *out = g_static_addr[dev];
   }
-  *out = g_static_addr[dev];
-  return HICACHE_OK;
+  // the calling thread's copy stream and events (created once per thread)
+  return staged_resources_ready();
 }
 
 }  // namespace
@@ -359,13 +374,10 @@ extern "C" hicache_status hicache_backup_all_layers_static_staging(
                                       std::to_string(page_all_layers) +
                                       " bytes, above the " + std::to_string(kHalf) +
                                       "-byte half of the static staging array");
-  if (n == 0) {
-    Prepared pr;
-    return prepare(pools, num_pools, device_indices, host_indices, index_bits, n, &o,
-                   /*dest_is_device=*/false, false, 0, 0, &pr);
-  }
+  // The set-up runs before the empty-list return, so that a call with no
+  // pairs serves as the warm-up that takes this entry point's device memory.
   void* base = nullptr;
-  st = static_staging_address(&base);
+  st = static_staging_setup(&base);
   if (st != HICACHE_OK) return st;
   o.path = HICACHE_PATH_STAGED;
   o.staging[0] = base;
@@ -374,7 +386,7 @@ extern "C" hicache_status hicache_backup_all_layers_static_staging(
   Prepared pr;
   st = prepare(pools, num_pools, device_indices, host_indices, index_bits, n, &o,
                /*dest_is_device=*/false, false, 0, 0, &pr);
-  if (st != HICACHE_OK) return st;
+  if (st != HICACHE_OK || n == 0) return st;
   return staged_backup(pr.pools, pr.o, pr.idx, stream);
 }
 

@@ -207,6 +207,11 @@ hicache_status launch_checksum(const PoolInfo& pool, int32_t tensor, int32_t lay
                                const void* dev_idx, int32_t index_bits, int64_t n,
                                uint64_t* out, cudaStream_t stream);
 int device_sm_count();
+// Loads, on the current device, every instance of the row-copy kernel that the
+// staged all-layer backup can launch (static striding, no layer rows; both
+// index widths, segment capacities and chunk depths), so that later launches
+// place no more code in device memory.
+hicache_status load_staged_backup_kernels();
 void count_launch();
 int64_t kernel_launches();
 

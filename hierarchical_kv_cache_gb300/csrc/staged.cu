@@ -127,6 +127,11 @@ hicache_status need_pages(const IndexSet& idx, int32_t P, std::vector<int64_t>* 
 
 }  // namespace
 
+hicache_status staged_resources_ready() {
+  StagedRes* r = nullptr;
+  return get_res(&r);
+}
+
 bool host_page_groups(const void* host_idx, int32_t bits, int64_t n, int32_t page_size,
                       std::vector<int64_t>* pages) {
   const int64_t P = page_size;
@@ -166,16 +171,30 @@ hicache_status staged_backup(const std::vector<PoolInfo>& pools, const hicache_o
 
   HK_CUDA(cudaEventRecord(r->fork, stream), "cudaEventRecord(fork)");
   HK_CUDA(cudaStreamWaitEvent(copy, r->fork, 0), "cudaStreamWaitEvent(fork)");
+  // From here on every return joins the copy stream back into `stream`, also
+  // on failure: copies of earlier chunks may still be in flight, and the next
+  // call ordered on `stream` may reuse the staging buffers they read.
+  auto join = [&](hicache_status s) {
+    cudaError_t e = cudaEventRecord(r->join, copy);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, r->join, 0);
+    if (e != cudaSuccess && s == HICACHE_OK) s = cuda_fail(e, "staged backup join");
+    return s;
+  };
+#define HK_TRY(call, what)                                  \
+  do {                                                      \
+    const cudaError_t e_ = (call);                          \
+    if (e_ != cudaSuccess) return join(cuda_fail(e_, what)); \
+  } while (0)
   for (int64_t k = 0, g0 = 0; g0 < groups; ++k, g0 += lay.cap_pages) {
     const int b = int(k & 1);
     const int64_t g1 = std::min(groups, g0 + lay.cap_pages);
     // the DMA of chunk k-2 must have drained buffer b before the gather reuses it
-    if (k >= 2) HK_CUDA(cudaStreamWaitEvent(stream, r->freed[b], 0), "cudaStreamWaitEvent(freed)");
+    if (k >= 2) HK_TRY(cudaStreamWaitEvent(stream, r->freed[b], 0), "cudaStreamWaitEvent(freed)");
     st = launch_rows(pools, side[b], idx.dev_gpu, nullptr, idx.bits, g0 * P, (g1 - g0) * P,
                      kDevToPaged, 0, L, cfg, stream);
-    if (st != HICACHE_OK) return st;
-    HK_CUDA(cudaEventRecord(r->ready[b], stream), "cudaEventRecord(ready)");
-    HK_CUDA(cudaStreamWaitEvent(copy, r->ready[b], 0), "cudaStreamWaitEvent(ready)");
+    if (st != HICACHE_OK) return join(st);
+    HK_TRY(cudaEventRecord(r->ready[b], stream), "cudaEventRecord(ready)");
+    HK_TRY(cudaStreamWaitEvent(copy, r->ready[b], 0), "cudaStreamWaitEvent(ready)");
     for (size_t p = 0; p < pools.size(); ++p) {
       const PoolInfo& pi = pools[p];
       const int64_t page_bytes = int64_t(L) * pi.P * pi.token_bytes;  // one host page, all layers
@@ -185,17 +204,16 @@ hicache_status staged_backup(const std::vector<PoolInfo>& pools, const hicache_o
           while (e < g1 && hp[size_t(e)] == hp[size_t(e - 1)] + 1) ++e;
           char* dst = pi.host[size_t(t)] + hp[size_t(j)] * page_bytes;
           const char* src = side[b].base[p][size_t(t)] + (j - g0) * page_bytes;
-          HK_CUDA(cudaMemcpyAsync(dst, src, size_t((e - j) * page_bytes), cudaMemcpyDeviceToHost, copy),
-                  "cudaMemcpyAsync(staging -> host)");
+          HK_TRY(cudaMemcpyAsync(dst, src, size_t((e - j) * page_bytes), cudaMemcpyDeviceToHost, copy),
+                 "cudaMemcpyAsync(staging -> host)");
           j = e;
         }
       }
     }
-    HK_CUDA(cudaEventRecord(r->freed[b], copy), "cudaEventRecord(freed)");
+    HK_TRY(cudaEventRecord(r->freed[b], copy), "cudaEventRecord(freed)");
   }
-  HK_CUDA(cudaEventRecord(r->join, copy), "cudaEventRecord(join)");
-  HK_CUDA(cudaStreamWaitEvent(stream, r->join, 0), "cudaStreamWaitEvent(join)");
-  return HICACHE_OK;
+#undef HK_TRY
+  return join(HICACHE_OK);
 }
 
 // The copy engine costs about 4 microseconds per copy on GB300, whatever the
@@ -221,8 +239,17 @@ hicache_status staged_load(const std::vector<PoolInfo>& pools, const hicache_opt
   const int32_t L = pools[0].L;
   const int32_t count = layer_end - layer_begin;
   int32_t recorded = 0;  // layer events recorded so far, in order
+  cudaStream_t forked = nullptr;  // the copy stream once it has forked from `stream`
+  StagedRes* r = nullptr;
   auto finish = [&](hicache_status s) {
-    // a failed load still completes every remaining layer event
+    // A failed load joins the copy stream back into `stream` (copies into the
+    // staging buffers may still be in flight) and then completes every
+    // remaining layer event.
+    if (forked) {
+      cudaError_t e = cudaEventRecord(r->join, forked);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, r->join, 0);
+      if (e != cudaSuccess && s == HICACHE_OK) s = cuda_fail(e, "staged load join");
+    }
     for (int32_t i = recorded; i < count; ++i)
       if (layer_done && layer_done[i]) cudaEventRecord(layer_done[i], stream);
     return s;
@@ -232,7 +259,6 @@ hicache_status staged_load(const std::vector<PoolInfo>& pools, const hicache_opt
   if (st != HICACHE_OK) return finish(st);
   if (layout_for(pools, o, 1).cap_pages < 1)
     return finish(fail(HICACHE_ENOSTAGE, "staging buffers hold less than one host page of one layer"));
-  StagedRes* r = nullptr;
   st = get_res(&r);
   if (st != HICACHE_OK) return finish(st);
   cudaStream_t copy = o.copy_stream ? o.copy_stream : r->copy;
@@ -252,6 +278,7 @@ hicache_status staged_load(const std::vector<PoolInfo>& pools, const hicache_opt
 
   HK_TRY(cudaEventRecord(r->fork, stream), "cudaEventRecord(fork)");
   HK_TRY(cudaStreamWaitEvent(copy, r->fork, 0), "cudaStreamWaitEvent(fork)");
+  forked = copy;
   int32_t first = layer_begin;
   if (count >= 2) {
     // The first layer of a burst is latency-critical, and through the copy

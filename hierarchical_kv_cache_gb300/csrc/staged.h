@@ -21,6 +21,10 @@ hicache_status staged_load(const std::vector<PoolInfo>& pools, const hicache_opt
                            const IndexSet& idx, int32_t layer_begin, int32_t layer_end,
                            cudaStream_t stream, cudaEvent_t* layer_done);
 
+// Creates, once per calling thread and current device, the copy stream and
+// events the staged path uses (later calls find them ready).
+hicache_status staged_resources_ready();
+
 // AUTO path choice for one call.
 hicache_path choose_path(const std::vector<PoolInfo>& pools, const hicache_opts& o,
                          const IndexSet& idx, Dir dir);

@@ -238,22 +238,31 @@ hicache_status hicache_load_burst(const hicache_pool* pools, int32_t num_pools,
  * or the CUDA allocator.  Same pairs, pools, result and errors as
  * hicache_backup_all_layers with HICACHE_PATH_STAGED, but the two staging
  * buffers are the halves of one device array of HICACHE_STATIC_STAGING_BYTES
- * that the library defines statically (every GPU that loads the library holds
- * it until the process exits).  The pages have no counterpart for this entry
- * point: it exists for callers that cannot allocate device memory at transfer
- * time, such as a serving engine that reserved all free HBM for its KV pool at
- * start-up, or a thin C caller with no device allocator of its own.
+ * that the library defines statically.  The pages have no counterpart for this
+ * entry point: it exists for callers that cannot allocate device memory at
+ * transfer time, such as a serving engine that reserved all free HBM for its KV
+ * pool at start-up, or a thin C caller with no device allocator of its own.
  *   - The call allocates nothing: no cudaMalloc, no cudaFree, no allocating
  *     library routine.  opts->staging and opts->staging_bytes are ignored.
+ *   - Warm-up: every call first makes sure, on the current device, that the
+ *     module holding the array is loaded (under CUDA's default lazy module
+ *     loading, that is when the array takes its 32 MiB of HBM), that the copy
+ *     kernels this call launches are loaded, and that the calling thread's copy
+ *     stream and events exist.  Only the first call on a device (and thread)
+ *     does any of this.  A call with n = 0 does this set-up and nothing else,
+ *     so a caller that is about to give the rest of HBM to its pools makes one
+ *     such call first (per device, with that device current, and on each
+ *     thread that will call it); later calls take no device memory.  Make that
+ *     first call before any stream capture.  With CUDA_MODULE_LOADING=EAGER
+ *     the array is placed in HBM when the library's module loads instead, and
+ *     stays there until the process exits either way.
+ *   - Do not call it on a device after cudaDeviceReset: the array's address
+ *     is resolved once per device and would then be stale.
  *   - Host-located indices covering whole host pages are required, as for the
  *     staged path (HICACHE_EINVAL otherwise).
  *   - One host page of all layers of all pools must fit in one 16 MiB half;
  *     larger pages are rejected with HICACHE_ENOSTAGE and a message giving both
  *     sizes.  Any number of pages is handled, 16 MiB at a time.
- *   - The first call on a device (with that device current) resolves the
- *     array's device address, and the first call on a thread and device creates
- *     the internal copy stream and events; make that first call before any
- *     stream capture.
  *   - Every call uses the same array.  Nothing in it needs to start at zero:
  *     each call writes every staging byte it copies out.  Calls that overlap on
  *     the GPU (for example on two streams without ordering) race on the array.
