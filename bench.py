@@ -8,10 +8,13 @@ is KV transfer GB/s (payload bytes of both operations / device time) and its
 fraction of the host-link peak measured in the same run with pinned
 cudaMemcpyAsync copies (D2H and H2D, 1 GiB, best of 5).
 
-Default workload: the Llama-3-8B-shaped MHA pool (32 layers, 8x128 bf16 K/V,
-page_size 64; backup of 256 pages = 2 GiB, then load-back of 256 pages =
-64 MiB per layer).  Pools are 8 GiB on each side, larger than L2, so no flush
-is needed between steps.
+Default workload: the 78-layer MLA model with two host pools (latent KV of
+576 bf16 per token plus the DSA indexer-K of 132 bytes per token, page_size
+64): an all-layer backup of 1024 pages (6.56 GB) and a load-back burst of 1024
+pages with 78 layer events (80.25 MiB per layer).  The pools hold 13.1 GB on
+each side, far larger than L2, so no flush is needed between steps.  After the
+timed region, a consumer kernel gated by each layer event reads that layer on
+another stream, to report how much of the consumers' work the burst hides.
 
 Multi-GPU: every pair is independent and each GPU holds its own pool replica,
 so N ranks run N independent replicas (weak scaling, no collective on the data
@@ -51,7 +54,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3, help="at least 3 (untimed)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="llama3_8b_mha")
+    ap.add_argument("--workload", default="mla78_dsa")
     ap.add_argument("--path", choices=["auto", "zero_copy", "staged"], default="auto")
     ap.add_argument("--staging-mib", type=int, default=256)
     ap.add_argument("--max-ctas", type=int, default=0)
@@ -60,8 +63,9 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--duplex", action="store_true",
                     help="also measure backup and load-back running concurrently (full duplex)")
-    ap.add_argument("--consumer", action="store_true",
-                    help="also measure a consumer kernel gated by each layer event (config 3)")
+    ap.add_argument("--no-consumer", action="store_true",
+                    help="skip the consumer kernels gated by each layer event (run after the "
+                         "timed region by default)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--out", default=None, help="also append the JSON line to this file")
@@ -530,7 +534,7 @@ def run_ours(args, rank, world):
         duplex = run_duplex(hk, pools, wl, idx_b, L, opts, opts_l, n)
 
     consumer = None
-    if args.consumer:
+    if not args.no_consumer:
         consumer = run_consumer_overlap(hk, pools, idx_l, opts, L, stream, bytes_layer)
 
     e2e = None
@@ -541,6 +545,9 @@ def run_ours(args, rank, world):
     res = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(total_ms / K, 4), "higher_is_better": True,
+        "first_layer_event_us": round(first_us, 1),
+        "first_event_bound_us": round(bound_us, 1),
+        "first_event_within_bound": first_us <= bound_us,
         "scaling": "weak", "vs_baseline": None, "dtype": "u8",
         "data": "synthetic (seeded bf16 ~N(0,1) pools, seeded random page lists)",
         "config": {
@@ -717,7 +724,7 @@ def run_consumer_overlap(hk, pools, idx_l, opts, L, stream, bytes_layer, reps=5)
     dev_idx = idx_l[1] if idx_l[1].is_cuda else idx_l[1].cuda()
     hk.hicache_layer_checksum(pool0, 0, 0, dev_idx, sums[0:1], stream=cons)  # load the module
     torch.cuda.synchronize()
-    lag, hidden, burst_ms, alone_ms = [], [], [], []
+    lag, hidden, burst_ms, alone_ms, early = [], [], [], [], []
     for _ in range(reps):
         torch.cuda.synchronize()
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(L)]
@@ -734,6 +741,8 @@ def run_consumer_overlap(hk, pools, idx_l, opts, L, stream, bytes_layer, reps=5)
             done[l].record(cons)
         torch.cuda.synchronize()
         lag.append(statistics.mean(evs[l].elapsed_time(done[l]) for l in range(L)) * 1e3)
+        # consumers that finished while the burst was still loading later layers
+        early.append(sum(1 for l in range(L - 1) if done[l].elapsed_time(evs[-1]) > 0))
         burst = t0.elapsed_time(evs[-1])
         total = t0.elapsed_time(done[-1])
         # the consumers alone, back to back on loaded data
@@ -754,6 +763,8 @@ def run_consumer_overlap(hk, pools, idx_l, opts, L, stream, bytes_layer, reps=5)
             "burst_ms": round(statistics.median(burst_ms), 4),
             "consumers_alone_ms": round(statistics.median(alone_ms), 4),
             "fraction_of_consumer_work_hidden": round(statistics.median(hidden), 4),
+            "consumers_done_before_last_layer_event": int(statistics.median(early)),
+            "layers": L,
             "reps": reps}
 
 
