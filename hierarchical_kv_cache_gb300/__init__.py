@@ -7,6 +7,7 @@ allocation helpers.  Build the library with ``hierarchical_kv_cache_gb300.build.
 from ._binding import (  # noqa: F401
     HICACHE_DEVERR_PAGE_ALIGN,
     HICACHE_DEVERR_RANGE,
+    HICACHE_DEVERR_TIMEOUT,
     HICACHE_EALIGN,
     HICACHE_ECUDA,
     HICACHE_EDUP,

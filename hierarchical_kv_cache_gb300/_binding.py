@@ -25,7 +25,7 @@ STATUS_NAMES = {0: "HICACHE_OK", 1: "HICACHE_EINVAL", 2: "HICACHE_ERANGE", 3: "H
 HICACHE_PATH_AUTO, HICACHE_PATH_ZERO_COPY, HICACHE_PATH_STAGED = 0, 1, 2
 HICACHE_INDEX_HOST, HICACHE_INDEX_DEVICE = 0, 1
 HICACHE_LAYOUT_PAGE_FIRST_DIRECT, HICACHE_LAYOUT_PAGE_FIRST = 0, 1
-HICACHE_DEVERR_RANGE, HICACHE_DEVERR_PAGE_ALIGN = 1, 2
+HICACHE_DEVERR_RANGE, HICACHE_DEVERR_PAGE_ALIGN, HICACHE_DEVERR_TIMEOUT = 1, 2, 4
 
 
 class c_pool(ctypes.Structure):

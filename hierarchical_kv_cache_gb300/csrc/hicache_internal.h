@@ -203,14 +203,28 @@ hicache_status launch_rows(const std::vector<PoolInfo>& pools, const SideSpec& s
                            int64_t pair_begin, int64_t npairs, Dir dir, int32_t layer_begin,
                            int32_t layer_end, const LaunchCfg& cfg, cudaStream_t stream,
                            const BurstWords* signal = nullptr);
+// Page-block copies (block_copy.cu): whole (page, layer) blocks of P * R bytes
+// between the device pool and HBM staging, with bulk-copy (TMA) loads and
+// stores.  Usable for pool `p` of `staging` when page_blocks_ok holds and every
+// page's P device slots are consecutive (checked by the caller).  Moves pages
+// [page_begin, page_begin + pages) of the pair list (the pair of page k's
+// first token is k * P) for layers [layer_begin, layer_end).
+bool page_blocks_ok(const PoolInfo& pi, const SideSpec& staging, size_t p);
+hicache_status launch_page_blocks(const std::vector<PoolInfo>& pools, const SideSpec& staging,
+                                  const void* dev_idx, int32_t index_bits, int64_t page_begin,
+                                  int64_t pages, Dir dir, int32_t layer_begin, int32_t layer_end,
+                                  const LaunchCfg& cfg, cudaStream_t stream);
+// Loads every instance of the page-block kernel on the current device.
+hicache_status load_block_kernels();
 hicache_status launch_checksum(const PoolInfo& pool, int32_t tensor, int32_t layer,
                                const void* dev_idx, int32_t index_bits, int64_t n,
                                uint64_t* out, cudaStream_t stream);
 int device_sm_count();
-// Loads, on the current device, every instance of the row-copy kernel that the
-// staged all-layer backup can launch (static striding, no layer rows; both
-// index widths, segment capacities and chunk depths), so that later launches
-// place no more code in device memory.
+// Loads, on the current device, every kernel instance that the staged
+// all-layer backup can launch: the row-copy kernel with static striding (both
+// index widths and segment capacities; 16- and 4-byte chunks; layer rows, for
+// a small pool backed up zero-copy beside the staged ones) and the page-block
+// kernel, so that later launches place no more code in device memory.
 hicache_status load_staged_backup_kernels();
 void count_launch();
 int64_t kernel_launches();

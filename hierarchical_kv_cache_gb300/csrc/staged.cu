@@ -125,6 +125,83 @@ hicache_status need_pages(const IndexSet& idx, int32_t P, std::vector<int64_t>* 
   return HICACHE_OK;
 }
 
+// Entries `which` of a pool list and of a side built over it.
+std::vector<PoolInfo> pick(const std::vector<PoolInfo>& pools, const std::vector<size_t>& which) {
+  std::vector<PoolInfo> out;
+  for (size_t p : which) out.push_back(pools[p]);
+  return out;
+}
+
+SideSpec pick(const SideSpec& s, const std::vector<size_t>& which) {
+  SideSpec out;
+  out.layer_origin = s.layer_origin;
+  for (size_t p : which) {
+    out.vec16.push_back(s.vec16[p]);
+    out.base.push_back(s.base[p]);
+    out.layer_stride.push_back(s.layer_stride[p]);
+    out.page_stride.push_back(s.page_stride[p]);
+    out.paged_tokens.push_back(s.paged_tokens[p]);
+    out.rows_per_page.push_back(s.rows_per_page[p]);
+  }
+  return out;
+}
+
+// True when the P device slots of every page group are consecutive, so that a
+// (page, layer) block is one contiguous span of the device layer buffer.
+bool device_pages_consecutive(const void* dev_idx, int32_t bits, int64_t n, int32_t P) {
+  for (int64_t k = 0; k < n; k += P) {
+    const int64_t d0 = bits == 32 ? at<int32_t>(dev_idx, k) : at<int64_t>(dev_idx, k);
+    for (int64_t t = 1; t < P; ++t) {
+      const int64_t d = bits == 32 ? at<int32_t>(dev_idx, k + t) : at<int64_t>(dev_idx, k + t);
+      if (d != d0 + t) return false;
+    }
+  }
+  return true;
+}
+
+// A pool whose host page of all layers (one tensor) is below this many bytes
+// moves zero-copy in a staged call that also holds a larger pool: one DMA per
+// host page would cost it more in the copy engine's fixed time per copy
+// (about 2.4 us device-to-host, 3.3 us host-to-device on GB300) than in
+// moving its bytes.  The DSA indexer of a 78-layer model (78 x 64 x 132 B =
+// 659 KB per page) is such a pool beside its 5.75 MB latent pages.
+constexpr int64_t kDirectPageBytes = int64_t(1) << 20;
+
+// Splits a staged call's pools into those that go through staging and the
+// small ones that move zero-copy beside them.
+void split_pools(const std::vector<PoolInfo>& pools, std::vector<size_t>* staged,
+                 std::vector<size_t>* direct) {
+  int64_t largest = 0;
+  std::vector<int64_t> page(pools.size());
+  for (size_t p = 0; p < pools.size(); ++p) {
+    page[p] = int64_t(pools[p].L) * pools[p].P * pools[p].token_bytes;
+    largest = std::max(largest, page[p]);
+  }
+  for (size_t p = 0; p < pools.size(); ++p)
+    (page[p] < kDirectPageBytes && page[p] < largest ? direct : staged)->push_back(p);
+}
+
+// Moves pages [g0, g1) of the pair list for layers [l0, l1) between the device
+// slots of `pools` and the staging `side`: whole (page, layer) blocks by bulk
+// copy where the pool allows it, rows otherwise.
+hicache_status move_staging(const std::vector<PoolInfo>& pools, const SideSpec& side,
+                            const IndexSet& idx, bool dev_consecutive, int64_t g0, int64_t g1,
+                            Dir dir, int32_t l0, int32_t l1, const LaunchCfg& cfg,
+                            cudaStream_t stream) {
+  const int32_t P = pools[0].P;
+  std::vector<size_t> blocks, rows;
+  for (size_t p = 0; p < pools.size(); ++p)
+    (dev_consecutive && page_blocks_ok(pools[p], side, p) ? blocks : rows).push_back(p);
+  hicache_status st = HICACHE_OK;
+  if (!blocks.empty())
+    st = launch_page_blocks(pick(pools, blocks), pick(side, blocks), idx.dev_gpu, idx.bits, g0,
+                            g1 - g0, dir, l0, l1, cfg, stream);
+  if (st == HICACHE_OK && !rows.empty())
+    st = launch_rows(pick(pools, rows), pick(side, rows), idx.dev_gpu, nullptr, idx.bits, g0 * P,
+                     (g1 - g0) * P, dir, l0, l1, cfg, stream);
+  return st;
+}
+
 }  // namespace
 
 hicache_status staged_resources_ready() {
@@ -150,13 +227,17 @@ bool host_page_groups(const void* host_idx, int32_t bits, int64_t n, int32_t pag
   return true;
 }
 
-hicache_status staged_backup(const std::vector<PoolInfo>& pools, const hicache_opts& o,
+hicache_status staged_backup(const std::vector<PoolInfo>& all_pools, const hicache_opts& o,
                              const IndexSet& idx, cudaStream_t stream) {
-  const int32_t P = pools[0].P;
-  const int32_t L = pools[0].L;
+  const int32_t P = all_pools[0].P;
+  const int32_t L = all_pools[0].L;
   std::vector<int64_t> hp;
   hicache_status st = need_pages(idx, P, &hp);
   if (st != HICACHE_OK) return st;
+  std::vector<size_t> staged_ids, direct_ids;
+  split_pools(all_pools, &staged_ids, &direct_ids);
+  const std::vector<PoolInfo> pools = pick(all_pools, staged_ids);
+  const std::vector<PoolInfo> direct = pick(all_pools, direct_ids);
   const StagingLayout lay = layout_for(pools, o, L);
   if (lay.cap_pages < 1)
     return fail(HICACHE_ENOSTAGE, "staging buffers hold less than one host page of all layers");
@@ -166,6 +247,7 @@ hicache_status staged_backup(const std::vector<PoolInfo>& pools, const hicache_o
   cudaStream_t copy = o.copy_stream ? o.copy_stream : r->copy;
   const LaunchCfg cfg{o.max_ctas, o.device_error, /*paged_in_hbm=*/true};
   const int64_t groups = int64_t(hp.size());
+  const bool dev_consecutive = device_pages_consecutive(idx.dev_cpu, idx.bits, idx.n, P);
   const SideSpec side[2] = {staging_side(pools, lay, static_cast<char*>(o.staging[0]), L, 0),
                             staging_side(pools, lay, static_cast<char*>(o.staging[1]), L, 0)};
 
@@ -190,11 +272,16 @@ hicache_status staged_backup(const std::vector<PoolInfo>& pools, const hicache_o
     const int64_t g1 = std::min(groups, g0 + lay.cap_pages);
     // the DMA of chunk k-2 must have drained buffer b before the gather reuses it
     if (k >= 2) HK_TRY(cudaStreamWaitEvent(stream, r->freed[b], 0), "cudaStreamWaitEvent(freed)");
-    st = launch_rows(pools, side[b], idx.dev_gpu, nullptr, idx.bits, g0 * P, (g1 - g0) * P,
-                     kDevToPaged, 0, L, cfg, stream);
+    st = move_staging(pools, side[b], idx, dev_consecutive, g0, g1, kDevToPaged, 0, L, cfg, stream);
     if (st != HICACHE_OK) return join(st);
     HK_TRY(cudaEventRecord(r->ready[b], stream), "cudaEventRecord(ready)");
     HK_TRY(cudaStreamWaitEvent(copy, r->ready[b], 0), "cudaStreamWaitEvent(ready)");
+    if (k == 0 && !direct.empty()) {
+      // the small pools, zero-copy, while the copy engine drains the first chunk
+      st = launch_rows(direct, host_side(direct), idx.dev_gpu, idx.host_gpu, idx.bits, 0, idx.n,
+                       kDevToPaged, 0, L, LaunchCfg{o.max_ctas, o.device_error}, stream);
+      if (st != HICACHE_OK) return join(st);
+    }
     for (size_t p = 0; p < pools.size(); ++p) {
       const PoolInfo& pi = pools[p];
       const int64_t page_bytes = int64_t(L) * pi.P * pi.token_bytes;  // one host page, all layers
@@ -216,27 +303,29 @@ hicache_status staged_backup(const std::vector<PoolInfo>& pools, const hicache_o
   return join(HICACHE_OK);
 }
 
-// The copy engine costs about 4 microseconds per copy on GB300, whatever the
+// The copy engine costs about 3 microseconds per copy on GB300, whatever the
 // number of streams or host threads issuing them: a 128 KiB copy (one layer of
 // one 64-token page of 2 KiB rows) moves 33 GB/s, a 512 KiB copy 106 GB/s,
 // 2 MiB 170 GB/s and 4 MiB 186 GB/s (host to device).  The staged load
 // therefore copies a group of consecutive layers of each host page per DMA
-// (they are adjacent in a page-first host page) and lets the groups grow
-// 1, 2, 4, ... layers until one copy carries about this many bytes, so that
-// the first layer still lands after one layer's transfer.  A 32-layer burst
-// runs as groups of 1, 2, 4, 8 and 17 layers.
+// (they are adjacent in a page-first host page).  The groups grow fourfold,
+// 4, 16, ... layers after the first layer (read zero-copy), until one copy
+// carries about this many bytes; a tail shorter than its group is merged or
+// split evenly.  A 32-layer burst of 128 KiB blocks runs as 1, 4 and 27
+// layers, a 78-layer burst of 72 KiB blocks as 1, 4, 16, 29 and 28.
 constexpr int64_t kDmaCopyTargetBytes = int64_t(4) << 20;
+constexpr int32_t kGroupGrowth = 4;
 // A group too large for the staging to hold every page at once moves in
 // chunks of pages; a chunk holds at least this many pages (or all of them),
 // so that the per-chunk scatter launch and stream hand-offs stay small next
 // to its copies.
 constexpr int64_t kMinChunkPages = 32;
 
-hicache_status staged_load(const std::vector<PoolInfo>& pools, const hicache_opts& o,
+hicache_status staged_load(const std::vector<PoolInfo>& all_pools, const hicache_opts& o,
                            const IndexSet& idx, int32_t layer_begin, int32_t layer_end,
                            cudaStream_t stream, cudaEvent_t* layer_done) {
-  const int32_t P = pools[0].P;
-  const int32_t L = pools[0].L;
+  const int32_t P = all_pools[0].P;
+  const int32_t L = all_pools[0].L;
   const int32_t count = layer_end - layer_begin;
   int32_t recorded = 0;  // layer events recorded so far, in order
   cudaStream_t forked = nullptr;  // the copy stream once it has forked from `stream`
@@ -257,14 +346,21 @@ hicache_status staged_load(const std::vector<PoolInfo>& pools, const hicache_opt
   std::vector<int64_t> hp;
   hicache_status st = need_pages(idx, P, &hp);
   if (st != HICACHE_OK) return finish(st);
+  std::vector<size_t> staged_ids, direct_ids;
+  split_pools(all_pools, &staged_ids, &direct_ids);
+  const std::vector<PoolInfo> pools = pick(all_pools, staged_ids);
+  const std::vector<PoolInfo> direct = pick(all_pools, direct_ids);
+  const SideSpec direct_side = host_side(direct);
   if (layout_for(pools, o, 1).cap_pages < 1)
     return finish(fail(HICACHE_ENOSTAGE, "staging buffers hold less than one host page of one layer"));
   st = get_res(&r);
   if (st != HICACHE_OK) return finish(st);
   cudaStream_t copy = o.copy_stream ? o.copy_stream : r->copy;
   const LaunchCfg cfg{o.max_ctas, o.device_error, /*paged_in_hbm=*/true};
+  const LaunchCfg zero_copy{o.max_ctas, o.device_error, /*paged_in_hbm=*/false};
   const int64_t groups = int64_t(hp.size());
   if (groups == 0) return finish(HICACHE_OK);  // nothing to move; the events still fire
+  const bool dev_consecutive = device_pages_consecutive(idx.dev_cpu, idx.bits, idx.n, P);
   int64_t max_block = 1;
   for (const PoolInfo& pi : pools) max_block = std::max(max_block, int64_t(pi.P) * pi.token_bytes);
   const int32_t g_cap = int32_t(std::min<int64_t>(
@@ -285,27 +381,32 @@ hicache_status staged_load(const std::vector<PoolInfo>& pools, const hicache_opt
     // engine it would cost one small copy per host page before its event.  It
     // is read zero-copy instead (the SMs read the host pool directly), while
     // the copy stream already moves the next group.
-    const LaunchCfg direct{o.max_ctas, o.device_error, /*paged_in_hbm=*/false};
-    st = launch_rows(pools, host_side(pools), idx.dev_gpu, idx.host_gpu, idx.bits, 0, idx.n,
-                     kPagedToDev, layer_begin, layer_begin + 1, direct, stream);
+    st = launch_rows(all_pools, host_side(all_pools), idx.dev_gpu, idx.host_gpu, idx.bits, 0,
+                     idx.n, kPagedToDev, layer_begin, layer_begin + 1, zero_copy, stream);
     if (st != HICACHE_OK) return finish(st);
     if (layer_done && layer_done[0])
       HK_TRY(cudaEventRecord(layer_done[0], stream), "cudaEventRecord(layer_done)");
     recorded = 1;
     first = layer_begin + 1;
   }
+  // The small pools' share of a scatter step: zero-copy from the host pool.
+  auto move_direct = [&](int64_t g0, int64_t g1, int32_t l0, int32_t l1) {
+    if (direct.empty()) return HICACHE_OK;
+    return launch_rows(direct, direct_side, idx.dev_gpu, idx.host_gpu, idx.bits, g0 * P,
+                       (g1 - g0) * P, kPagedToDev, l0, l1, zero_copy, stream);
+  };
   int64_t step = 0;
-  int32_t g_want = first == layer_begin ? 1 : 2;
+  int32_t g_want = first == layer_begin ? 1 : std::min(g_cap, kGroupGrowth);
   for (int32_t l = first, g = 1; l < layer_end; l += g) {
-    // the next group size; a tail shorter than the group joins it rather
-    // than paying for small copies of its own
-    g = std::min(g_want, layer_end - l);
-    const int32_t rest = layer_end - l - g;
-    if (rest > 0 && rest < g && g + rest <= g_cap) g += rest;
+    // the next group size; a tail shorter than the group joins it (or, when
+    // both would not fit in one copy, the rest is split in two even groups)
+    const int32_t remaining = layer_end - l;
+    g = std::min(g_want, remaining);
+    if (remaining > g && remaining - g < g) g = remaining <= g_cap ? remaining : (remaining + 1) / 2;
     // the largest such group whose chunks hold kMinChunkPages pages, or every
     // page; one layer per group when not even that fits
     while (g > 1 && layout_for(pools, o, g).cap_pages < std::min(groups, kMinChunkPages)) --g;
-    g_want = std::min(g_cap, 2 * g_want);
+    g_want = std::min(g_cap, kGroupGrowth * g_want);
     const StagingLayout lay = layout_for(pools, o, g);
     for (int64_t g0 = 0; g0 < groups; g0 += lay.cap_pages, ++step) {
       const int b = int(step & 1);
@@ -319,7 +420,7 @@ hicache_status staged_load(const std::vector<PoolInfo>& pools, const hicache_opt
         const int64_t R = pi.token_bytes;
         const int64_t block = int64_t(pi.P) * R;  // one (page, layer) block
         const int64_t host_page = block * L;
-        const bool direct = pi.layout == HICACHE_LAYOUT_PAGE_FIRST_DIRECT;
+        const bool direct_layout = pi.layout == HICACHE_LAYOUT_PAGE_FIRST_DIRECT;
         for (int32_t t = 0; t < pi.T; ++t) {
           for (int64_t j = g0; j < g1;) {
             int64_t e = j + 1;
@@ -330,12 +431,13 @@ hicache_status staged_load(const std::vector<PoolInfo>& pools, const hicache_opt
             // host_page apart; page_first: they are contiguous per token, tokens
             // L * R apart
             const cudaError_t ce =
-                direct ? cudaMemcpy2DAsync(dst, size_t(block * g), page0 + int64_t(l) * block,
-                                           size_t(host_page), size_t(block * g), size_t(e - j),
-                                           cudaMemcpyHostToDevice, copy)
-                       : cudaMemcpy2DAsync(dst, size_t(R * g), page0 + int64_t(l) * R,
-                                           size_t(L) * size_t(R), size_t(R * g),
-                                           size_t((e - j) * pi.P), cudaMemcpyHostToDevice, copy);
+                direct_layout
+                    ? cudaMemcpy2DAsync(dst, size_t(block * g), page0 + int64_t(l) * block,
+                                        size_t(host_page), size_t(block * g), size_t(e - j),
+                                        cudaMemcpyHostToDevice, copy)
+                    : cudaMemcpy2DAsync(dst, size_t(R * g), page0 + int64_t(l) * R,
+                                        size_t(L) * size_t(R), size_t(R * g),
+                                        size_t((e - j) * pi.P), cudaMemcpyHostToDevice, copy);
             HK_TRY(ce, "cudaMemcpy2DAsync(host -> staging)");
             j = e;
           }
@@ -344,14 +446,16 @@ hicache_status staged_load(const std::vector<PoolInfo>& pools, const hicache_opt
       HK_TRY(cudaEventRecord(r->ready[b], copy), "cudaEventRecord(ready)");
       HK_TRY(cudaStreamWaitEvent(stream, r->ready[b], 0), "cudaStreamWaitEvent(ready)");
       if (!last_chunk) {
-        st = launch_rows(pools, side, idx.dev_gpu, nullptr, idx.bits, g0 * P, (g1 - g0) * P,
-                         kPagedToDev, l, l + g, cfg, stream);
+        st = move_staging(pools, side, idx, dev_consecutive, g0, g1, kPagedToDev, l, l + g, cfg,
+                          stream);
+        if (st == HICACHE_OK) st = move_direct(g0, g1, l, l + g);
         if (st != HICACHE_OK) return finish(st);
       } else {
         // the group's last chunk: scatter layer by layer, each followed by its event
         for (int32_t k = l; k < l + g; ++k) {
-          st = launch_rows(pools, side, idx.dev_gpu, nullptr, idx.bits, g0 * P, (g1 - g0) * P,
-                           kPagedToDev, k, k + 1, cfg, stream);
+          st = move_staging(pools, side, idx, dev_consecutive, g0, g1, kPagedToDev, k, k + 1, cfg,
+                            stream);
+          if (st == HICACHE_OK) st = move_direct(g0, g1, k, k + 1);
           if (st != HICACHE_OK) return finish(st);
           if (layer_done && layer_done[k - layer_begin])
             HK_TRY(cudaEventRecord(layer_done[k - layer_begin], stream), "cudaEventRecord(layer_done)");

@@ -85,29 +85,30 @@ hicache_status launch_segments(const CopyParams<MAXSEG>& prm, int32_t index_bits
 namespace {
 std::atomic<int64_t> g_launches{0};
 
-template <typename IdxT, int MAXSEG, bool DEEP4>
+template <typename IdxT, int MAXSEG, bool LAYER_ROWS, bool DEEP4>
 cudaError_t load_static_instance() {
   cudaFuncAttributes a{};
-  return cudaFuncGetAttributes(&a, row_copy_kernel<IdxT, MAXSEG, false, false, DEEP4>);
+  return cudaFuncGetAttributes(&a, row_copy_kernel<IdxT, MAXSEG, false, LAYER_ROWS, DEEP4>);
+}
+
+template <typename IdxT, int MAXSEG>
+cudaError_t load_static_instances() {
+  cudaError_t e = load_static_instance<IdxT, MAXSEG, false, false>();
+  if (e == cudaSuccess) e = load_static_instance<IdxT, MAXSEG, false, true>();
+  if (e == cudaSuccess) e = load_static_instance<IdxT, MAXSEG, true, false>();
+  return e;
 }
 }  // namespace
 
 hicache_status load_staged_backup_kernels() {
   // Under CUDA's lazy module loading a kernel is loaded, and its code placed
   // in device memory, at its first use; querying its attributes is such a use.
-  const cudaError_t es[] = {
-      load_static_instance<int32_t, kMaxSegSmall, false>(),
-      load_static_instance<int32_t, kMaxSegSmall, true>(),
-      load_static_instance<int32_t, kMaxSegLarge, false>(),
-      load_static_instance<int32_t, kMaxSegLarge, true>(),
-      load_static_instance<int64_t, kMaxSegSmall, false>(),
-      load_static_instance<int64_t, kMaxSegSmall, true>(),
-      load_static_instance<int64_t, kMaxSegLarge, false>(),
-      load_static_instance<int64_t, kMaxSegLarge, true>(),
-  };
-  for (cudaError_t e : es)
-    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncGetAttributes(row copy kernel)");
-  return HICACHE_OK;
+  cudaError_t e = load_static_instances<int32_t, kMaxSegSmall>();
+  if (e == cudaSuccess) e = load_static_instances<int32_t, kMaxSegLarge>();
+  if (e == cudaSuccess) e = load_static_instances<int64_t, kMaxSegSmall>();
+  if (e == cudaSuccess) e = load_static_instances<int64_t, kMaxSegLarge>();
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncGetAttributes(row copy kernel)");
+  return load_block_kernels();
 }
 
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }

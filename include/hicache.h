@@ -124,6 +124,8 @@ typedef enum hicache_layout {
 /* Bits kernels OR into hicache_opts.device_error. */
 #define HICACHE_DEVERR_RANGE 1u     /* a pair was out of range and skipped */
 #define HICACHE_DEVERR_PAGE_ALIGN 2u /* a page-granular pair was not page-aligned and skipped */
+#define HICACHE_DEVERR_TIMEOUT 4u    /* a bulk copy of the staged path did not land within one
+                                        second; that launch stopped early (never expected) */
 
 typedef struct hicache_pool {
   int32_t num_layers;     /* L: layers of this pool */
