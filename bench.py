@@ -83,6 +83,19 @@ def parse_args():
     ap.add_argument("--sweep-layers", type=int, default=4)
     ap.add_argument("--dma-sweep", action="store_true",
                     help="measure the copy engine's cost per copy against the copy size instead")
+    ap.add_argument("--latency", action="store_true",
+                    help="measure per-op latency for small page counts instead")
+    ap.add_argument("--latency-pages", default="1,4,16,64,256")
+    ap.add_argument("--contention", action="store_true",
+                    help="measure both paths beside a bf16 GEMM loop that occupies the SMs "
+                         "(the regime the staged path is for) instead")
+    ap.add_argument("--contention-reps", type=int, default=3)
+    ap.add_argument("--contention-staged-ctas", default="0,38",
+                    help="copy CTA caps of the staged path under --contention")
+    ap.add_argument("--contention-alone-only", action="store_true",
+                    help="time the transfers alone only (no GEMM loop beside them)")
+    ap.add_argument("--contention-ctas", default="16,38,76,152,304",
+                    help="copy CTA caps to measure under contention (0 = library default)")
     return ap.parse_args()
 
 
@@ -295,9 +308,10 @@ def hbm_peak():
         return 6800.0
 
 
-def traffic_per_launch(which, algorithmic_bytes):
-    """DRAM bytes (read + write) per launch from the committed ncu record, scaled to this
-    launch's algorithmic bytes; None when the kernel source changed since the capture."""
+def traffic_per_launch(workload, which, algorithmic_bytes):
+    """DRAM bytes (read + write) per launch from the committed ncu record of this workload,
+    scaled to this launch's algorithmic bytes; None when the record has no such launch or
+    the kernel source changed since the capture."""
     import hashlib
     try:
         with open(os.path.join(REPO, "profiles", "row_copy_kernel_traffic.json")) as f:
@@ -307,7 +321,9 @@ def traffic_per_launch(which, algorithmic_bytes):
         return None
     if hashlib.sha256(src).hexdigest()[:16] != rec.get("source_sha256_16"):
         return None
-    c = rec["launches"][which]
+    c = rec.get("workloads", {}).get(workload, {}).get("launches", {}).get(which)
+    if c is None:
+        return None
     per_byte = (c["dram_read_bytes"] + c["dram_write_bytes"]) / c["algorithmic_bytes"]
     return int(per_byte * algorithmic_bytes)
 
@@ -443,9 +459,13 @@ def run_ours(args, rank, world):
     ht_h = torch.as_tensor(h).pin_memory()
     d2t_h = torch.as_tensor(d2).pin_memory()
     if args.path == "staged":
+        # the staged path plans its DMAs on the CPU: pinned host indices, which
+        # the library copies into HBM (opts.index_staging) for its kernels
         idx_b, idx_l = (dt_h, ht_h), (ht_h, d2t_h)
         opts = hk.Opts(path=path, index_location=hk.HICACHE_INDEX_HOST, staging=staging,
-                       max_ctas=args.max_ctas, device_error=err, burst_words=words)
+                       max_ctas=args.max_ctas, device_error=err, burst_words=words,
+                       index_staging=torch.empty(hk.index_staging_bytes(n, 64),
+                                                 dtype=torch.uint8, device="cuda"))
     else:
         idx_b, idx_l = (dt, ht_dev), (ht_dev, d2t)
         opts = hk.Opts(path=path, index_location=hk.HICACHE_INDEX_DEVICE, staging=staging,
@@ -514,6 +534,8 @@ def run_ours(args, rank, world):
     value = aggregate_gbs(world, K, step_bytes, total_ms)
 
     mb, ml = statistics.mean(t_backup), statistics.mean(t_load)
+    # the committed DRAM-traffic record is per workload, in its default host layout
+    traffic_key = args.workload + (f":{args.layout}" if args.layout else "")
     backup_gbs = bytes_backup / (mb * 1e-3) / GB
     load_gbs = bytes_load / (ml * 1e-3) / GB
     layer_gbs = bytes_layer / (statistics.median(per_layer) * 1e-3) / GB if per_layer else None
@@ -556,7 +578,8 @@ def run_ours(args, rank, world):
             "pages_per_op": wl.move_pages, "tokens_per_op": int(n), "layers": L,
             "step": "all-layer D2H backup + H2D per-layer load-back burst with layer events",
             "step_payload_bytes": int(step_bytes), "path": args.path, "burst": args.burst,
-            "index_location": "device (HBM)" if args.path != "staged" else "host (pinned)",
+            "index_location": ("device (HBM)" if args.path != "staged" else
+                               "host (pinned), copied by the call into opts.index_staging"),
             "l2": "inputs larger than L2 (pools of GiBs on each side), no flush",
             "parallelism": f"replicas x{world}",
             "host_alloc_s": round(t_alloc, 1),
@@ -589,7 +612,7 @@ def run_ours(args, rank, world):
             "bound": "host_link", "achieved": round(backup_gbs, 2), "peak": round(link["d2h"], 2),
             "unit": "GB/s", "frac": round(backup_gbs / link["d2h"], 4),
             "traffic": (None if staged else
-                        traffic_per_launch("backup_all_layers", bytes_backup)),
+                        traffic_per_launch(traffic_key, "backup_all_layers", bytes_backup)),
             "kernel": ("staged backup: gather kernels into two HBM staging buffers, then one "
                        "cudaMemcpyAsync per host-page run, whole operation"
                        if staged else
@@ -611,7 +634,8 @@ def run_ours(args, rank, world):
             "bound": "host_link", "achieved": round(layer_gbs, 2) if layer_gbs else None,
             "peak": round(link["h2d"], 2), "unit": "GB/s",
             "frac": round(layer_gbs / link["h2d"], 4) if layer_gbs else None,
-            "traffic": traffic_per_launch("load_one_layer" if args.burst == "per_layer"
+            "traffic": traffic_per_launch(traffic_key, "load_one_layer"
+                                          if args.burst == "per_layer"
                                           else "load_burst_signalling", bytes_layer),
             "kernel": ("row_copy_kernel<int64,16,8>: one per-layer load launch"
                        if args.burst == "per_layer" else
@@ -639,7 +663,7 @@ def run_ours(args, rank, world):
         res["roofline_burst"] = {
             "bound": "host_link", "achieved": round(rest_gbs, 2), "peak": round(link["h2d"], 2),
             "unit": "GB/s", "frac": round(rest_gbs / link["h2d"], 4),
-            "traffic": traffic_per_launch("load_burst_signalling", rest_bytes),
+            "traffic": traffic_per_launch(traffic_key, "load_burst_signalling", rest_bytes),
             "kernel": ("row_copy_kernel<int64,512,signalling>: the launch covering layers "
                        f"1..{L - 1} of the burst"
                        if bytes_layer >= SPLIT_FIRST_LAYER_BYTES else
@@ -1149,8 +1173,237 @@ def run_dma_sweep(args):
                 f.write(json.dumps(rec) + "\n")
 
 
+def run_latency(args, reps=30):
+    """Latency of one op for small page counts.
+
+    device: the op is enqueued behind a sleep kernel of about 0.2 ms on its
+    stream, so that the timing events around it hold its GPU work only, not the
+    host's enqueue (median of `reps`).  call-to-done: wall time from the call on
+    an idle stream to the end of a synchronize, what a caller waiting for the
+    op sees.  host enqueue: the call's own host time.  Ops: the all-layer
+    backup, one layer's load, and the whole load-back burst (single-launch, one
+    event per layer), with device-located indices, on the first k pages of the
+    workload's lists.
+    """
+    import torch
+    import hierarchical_kv_cache_gb300 as hk
+    from hierarchical_kv_cache_gb300 import pools as hpools
+    from hierarchical_kv_cache_gb300.build import build
+
+    build()
+    torch.cuda.set_device(0)
+    wl, d, h, d2 = build_workload(args.workload, args=args)
+    L = wl.pools[0].num_layers
+    P = wl.pools[0].page_size
+    pools = []
+    for i, sh in enumerate(wl.pools):
+        p = hpools.allocate_pool(sh)
+        hpools.fill_device_random_(p, wl.seed + i, sh.value_kind)
+        pools.append(p)
+    stream = torch.cuda.Stream()
+    words = torch.zeros(4 * L, dtype=torch.int32, device="cuda")
+    opts = hk.Opts(path=hk.HICACHE_PATH_ZERO_COPY, index_location=hk.HICACHE_INDEX_DEVICE,
+                   burst_words=words, max_ctas=args.max_ctas)
+    evs = [torch.cuda.Event() for _ in range(L)]
+    out = []
+    for k in [int(x) for x in args.latency_pages.split(",")]:
+        m = min(k, wl.move_pages) * P
+        dt = torch.as_tensor(d[:m]).cuda()
+        ht = torch.as_tensor(h[:m]).cuda()
+        d2t = torch.as_tensor(d2[:m]).cuda()
+        bytes_backup, bytes_layer = payload_bytes(wl, m)
+        ops = {"backup_all_layers": (bytes_backup, lambda: hk.hicache_backup_all_layers(
+                   pools, dt, ht, opts=opts, stream=stream)),
+               "load_one_layer": (bytes_layer, lambda: hk.hicache_load_layer(
+                   pools, 0, ht, d2t, opts=opts, stream=stream, layer_done=evs[0])),
+               "load_burst": (bytes_layer * L, lambda: hk.hicache_load_burst(
+                   pools, 0, L, ht, d2t, opts=opts, stream=stream, layer_done=evs))}
+        for name, (nbytes, fn) in ops.items():
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            dev_us, wall_us, enq_us = [], [], []
+            for _ in range(reps):
+                t0 = torch.cuda.Event(enable_timing=True)
+                t1 = torch.cuda.Event(enable_timing=True)
+                stream.synchronize()
+                with torch.cuda.stream(stream):
+                    torch.cuda._sleep(400_000)  # the op queues up behind it
+                t0.record(stream)
+                fn()
+                t1.record(stream)
+                t1.synchronize()
+                dev_us.append(t0.elapsed_time(t1) * 1e3)
+                stream.synchronize()
+                w0 = time.perf_counter()
+                fn()
+                w1 = time.perf_counter()
+                stream.synchronize()
+                wall_us.append((time.perf_counter() - w0) * 1e6)
+                enq_us.append((w1 - w0) * 1e6)
+            med = statistics.median(dev_us)
+            rec = {"workload": args.workload, "pages": m // P, "op": name, "bytes": int(nbytes),
+                   "device_us_p50": round(med, 2), "device_us_min": round(min(dev_us), 2),
+                   "call_to_done_us_p50": round(statistics.median(wall_us), 2),
+                   "host_enqueue_us_p50": round(statistics.median(enq_us), 2),
+                   "gbs": round(nbytes / (med * 1e-6) / GB, 2)}
+            out.append(rec)
+            print(json.dumps(rec), flush=True)
+    if args.out:
+        with open(args.out, "a") as f:
+            for rec in out:
+                f.write(json.dumps(rec) + "\n")
+
+
+def run_contention(args):
+    """Both paths beside compute that occupies the SMs (path choice, S5).
+
+    A bf16 GEMM loop (cuBLAS, 8192^3 per matmul) runs on its own stream for
+    the whole measurement.  For each path and copy CTA cap, the backup and the
+    load-back burst of the workload are timed alone and beside the GEMM loop,
+    and the GEMM throughput is timed alone and beside each transfer.  The
+    staged path moves its bytes with the copy engine and holds the SMs only for
+    its gather and scatter kernels; the zero-copy path holds them for the whole
+    transfer.
+    """
+    import torch
+    import hierarchical_kv_cache_gb300 as hk
+    from hierarchical_kv_cache_gb300 import pools as hpools
+    from hierarchical_kv_cache_gb300.build import build
+
+    build()
+    torch.cuda.set_device(0)
+    wl, d, h, d2 = build_workload(args.workload, args=args)
+    L = wl.pools[0].num_layers
+    n = d.size
+    pools = []
+    for i, sh in enumerate(wl.pools):
+        p = hpools.allocate_pool(sh)
+        hpools.fill_device_random_(p, wl.seed + i, sh.value_kind)
+        pools.append(p)
+    staging = [torch.empty(args.staging_mib << 20, dtype=torch.uint8, device="cuda")
+               for _ in range(2)]
+    idx_staging = torch.empty(hk.index_staging_bytes(n, 64), dtype=torch.uint8, device="cuda")
+    dt_h = torch.as_tensor(d).pin_memory()
+    ht_h = torch.as_tensor(h).pin_memory()
+    d2t_h = torch.as_tensor(d2).pin_memory()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    words = torch.zeros(4 * L, dtype=torch.int32, device="cuda")
+    bytes_backup, bytes_layer = payload_bytes(wl, n)
+    bytes_load = bytes_layer * L
+    link = measure_link_peak()
+    xfer_s = torch.cuda.Stream()
+    gemm_s = torch.cuda.Stream()
+    N = 8192
+    a = torch.randn(N, N, device="cuda", dtype=torch.bfloat16)
+    b = torch.randn(N, N, device="cuda", dtype=torch.bfloat16)
+    c = torch.empty(N, N, device="cuda", dtype=torch.bfloat16)
+    flops = 2.0 * N ** 3
+
+    def gemms(k):
+        with torch.cuda.stream(gemm_s):
+            for _ in range(k):
+                torch.matmul(a, b, out=c)
+
+    def timed_gemm(k):
+        """k GEMMs on gemm_s with an event before the first and after each."""
+        e0 = torch.cuda.Event(enable_timing=True)
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(k)]
+        e0.record(gemm_s)
+        with torch.cuda.stream(gemm_s):
+            for e in ends:
+                torch.matmul(a, b, out=c)
+                e.record(gemm_s)
+        return e0, ends
+
+    gemms(3)
+    torch.cuda.synchronize()
+    e0, ends = timed_gemm(20)
+    torch.cuda.synchronize()
+    gemm_ms = e0.elapsed_time(ends[-1]) / 20
+    gemm_alone = flops / (gemm_ms * 1e-3) / 1e12
+    def point(fn, nbytes, peak):
+        """One transfer op, alone and beside the GEMM loop."""
+        fn()
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(xfer_s)
+        for _ in range(3):
+            fn()
+        t1.record(xfer_s)
+        torch.cuda.synchronize()
+        alone_ms = t0.elapsed_time(t1) / 3
+        alone = nbytes / (alone_ms * 1e-3) / GB
+        if args.contention_alone_only:
+            return {"alone_gbs": round(alone, 2), "alone_frac_of_link": round(alone / peak, 4)}
+        # beside the GEMM loop: enough GEMMs to outlast the transfers even if
+        # they slow down fourfold
+        k = int(4 * 3 * alone_ms / gemm_ms) + 8
+        g0, ends = timed_gemm(k)
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        xfer_s.wait_event(g0)
+        t0.record(xfer_s)
+        for _ in range(3):
+            fn()
+        t1.record(xfer_s)
+        torch.cuda.synchronize()
+        window = t0.elapsed_time(t1)
+        busy_ms = window / 3
+        # GEMM throughput during the transfers: the GEMMs that ended inside
+        # the window, over the window
+        done = sum(1 for e in ends if 0.0 < t0.elapsed_time(e) <= window)
+        if int(err.item()) != 0:
+            raise RuntimeError(f"device error word {int(err.item())}")
+        beside = nbytes / (busy_ms * 1e-3) / GB
+        return {"alone_gbs": round(alone, 2), "beside_gemm_gbs": round(beside, 2),
+                "alone_frac_of_link": round(alone / peak, 4),
+                "beside_gemm_frac_of_link": round(beside / peak, 4),
+                "gemm_tflops_alone": round(gemm_alone, 1),
+                "gemm_tflops_during_transfers": round(done * flops / (window * 1e-3) / 1e12, 1),
+                "gemm_outlasted_transfers": bool(t0.elapsed_time(ends[-1]) > window),
+                "transfers_ms": round(window, 2)}
+
+    out = []
+    evs = [torch.cuda.Event() for _ in range(L)]
+    caps = [int(x) for x in args.contention_ctas.split(",")]
+    for path in ("zero_copy", "staged"):
+        for cap in (caps if path == "zero_copy"
+                    else [int(x) for x in args.contention_staged_ctas.split(",")]):
+            o = hk.Opts(path=hk.HICACHE_PATH_ZERO_COPY if path == "zero_copy"
+                        else hk.HICACHE_PATH_STAGED,
+                        index_location=hk.HICACHE_INDEX_HOST, staging=staging, max_ctas=cap,
+                        device_error=err, burst_words=words, index_staging=idx_staging)
+            ops = {"backup": (bytes_backup, link["d2h"],
+                              lambda: hk.hicache_backup_all_layers(pools, dt_h, ht_h, opts=o,
+                                                                   stream=xfer_s)),
+                   "burst": (bytes_load, link["h2d"],
+                             lambda: hk.hicache_load_burst(pools, 0, L, ht_h, d2t_h, opts=o,
+                                                           stream=xfer_s, layer_done=evs))}
+            for name, (nbytes, peak, fn) in ops.items():
+                for rep in range(args.contention_reps):
+                    rec = {"path": path, "max_ctas": cap, "op": name, "rep": rep,
+                           **point(fn, nbytes, peak)}
+                    out.append(rec)
+                    print(json.dumps(rec), flush=True)
+    if args.out:
+        with open(args.out, "w") as f:
+            for rec in out:
+                f.write(json.dumps(rec) + "\n")
+    print(json.dumps({"contention_points": len(out), "workload": wl.name,
+                      "link_peak_gbs": link, "gemm_tflops_alone": round(gemm_alone, 1)}),
+          flush=True)
+
+
 def main():
     args = parse_args()
+    if args.contention:
+        run_contention(args)
+        return
+    if args.latency:
+        run_latency(args)
+        return
     if args.sweep:
         run_sweep(args)
         return

@@ -17,7 +17,11 @@ from ._binding import (  # noqa: F401
     HICACHE_INDEX_DEVICE,
     HICACHE_INDEX_HOST,
     HICACHE_LAYOUT_PAGE_FIRST,
+    HICACHE_AUTO_STAGED_BELOW_CTAS_BACKUP,
+    HICACHE_AUTO_STAGED_BELOW_CTAS_LOAD,
     HICACHE_LAYOUT_PAGE_FIRST_DIRECT,
+    HICACHE_OP_BACKUP,
+    HICACHE_OP_LOAD,
     HICACHE_OK,
     HICACHE_PATH_AUTO,
     HICACHE_PATH_STAGED,
@@ -26,6 +30,7 @@ from ._binding import (  # noqa: F401
     Opts,
     Pool,
     abi_version,
+    hicache_auto_path,
     hicache_backup_all_layers,
     hicache_backup_all_layers_static_staging,
     hicache_check_pairs,

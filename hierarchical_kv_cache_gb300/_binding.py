@@ -25,6 +25,9 @@ STATUS_NAMES = {0: "HICACHE_OK", 1: "HICACHE_EINVAL", 2: "HICACHE_ERANGE", 3: "H
 HICACHE_PATH_AUTO, HICACHE_PATH_ZERO_COPY, HICACHE_PATH_STAGED = 0, 1, 2
 HICACHE_INDEX_HOST, HICACHE_INDEX_DEVICE = 0, 1
 HICACHE_LAYOUT_PAGE_FIRST_DIRECT, HICACHE_LAYOUT_PAGE_FIRST = 0, 1
+HICACHE_OP_BACKUP, HICACHE_OP_LOAD = 0, 1
+# copy-CTA budgets below which AUTO may take the staged path (include/hicache.h)
+HICACHE_AUTO_STAGED_BELOW_CTAS_BACKUP, HICACHE_AUTO_STAGED_BELOW_CTAS_LOAD = 24, 32
 HICACHE_DEVERR_RANGE, HICACHE_DEVERR_PAGE_ALIGN, HICACHE_DEVERR_TIMEOUT = 1, 2, 4
 
 
@@ -73,6 +76,9 @@ def lib():
                                         ctypes.POINTER(i64), ctypes.POINTER(i64)]
         L.hicache_layer_checksum.argtypes = [P, i32, i32, vp, i32, i64, vp, vp]
         L.hicache_check_pairs.argtypes = [P, i32, vp, vp, i32, i64, i32]
+        L.hicache_auto_path.argtypes = [P, i32, vp, vp, i32, i64, O, i32, i32,
+                                        ctypes.POINTER(i32)]
+        L.hicache_auto_path.restype = ctypes.c_int
         L.hicache_backup_all_layers_static_staging.argtypes = [P, i32, vp, vp, i32, i64, O, vp]
         L.hicache_backup_all_layers_static_staging.restype = ctypes.c_int
         for f in ("hicache_backup_all_layers", "hicache_load_layer", "hicache_load_burst",
@@ -327,6 +333,36 @@ def hicache_check_pairs(pools, device_indices, host_indices, *, dest_is_device: 
     _check(lib().hicache_check_pairs(arr, n, d.ctypes.data, h.ctypes.data, bits, d.size,
                                      int(bool(dest_is_device))))
     del keep  # the pointer arrays lived until the call returned
+
+
+def hicache_auto_path(pools, device_indices, host_indices, *, op: int, layers: int = 1,
+                      opts: Optional[Opts] = None) -> int:
+    """Path a call with opts.path AUTO takes (host only): HICACHE_PATH_ZERO_COPY or _STAGED.
+
+    Index arrays are numpy arrays (host memory; opts.index_location defaults to
+    HICACHE_INDEX_HOST) or torch tensors (location inferred as for the calls).
+    """
+    arr, npools, keep = _pools_arg(pools)
+    if isinstance(device_indices, np.ndarray) or isinstance(host_indices, np.ndarray):
+        d = np.ascontiguousarray(device_indices)
+        h = np.ascontiguousarray(host_indices)
+        if d.dtype != h.dtype or d.dtype not in (np.int32, np.int64) or d.shape != h.shape:
+            raise TypeError("index arrays must be equal-length int32 or int64")
+        bits, n, dp, hp = 32 if d.dtype == np.int32 else 64, d.size, d.ctypes.data, h.ctypes.data
+        o = opts or Opts()
+        if o.index_location is None:
+            from dataclasses import replace
+            o = replace(o, index_location=HICACHE_INDEX_HOST)
+        co = _opts_arg(o, None, None)
+    else:
+        bits, n = _indices(device_indices, host_indices)
+        dp, hp = device_indices.data_ptr(), host_indices.data_ptr()
+        co = _opts_arg(opts, device_indices, host_indices)
+    out = ctypes.c_int32(-1)
+    _check(lib().hicache_auto_path(arr, npools, dp, hp, bits, n, ctypes.byref(co), int(op),
+                                   int(layers), ctypes.byref(out)))
+    del keep  # the pointer arrays lived until the call returned
+    return out.value
 
 
 def hicache_layer_checksum(pool: Pool, tensor: int, layer: int, device_indices, out_sum, *,

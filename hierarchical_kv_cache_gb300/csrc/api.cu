@@ -201,9 +201,9 @@ hicache_status check_burst_words(const hicache_opts& o, int32_t count) {
 
 LaunchCfg launch_cfg(const hicache_opts& o) { return LaunchCfg{o.max_ctas, o.device_error}; }
 
-hicache_path resolve_path(const Prepared& pr, Dir dir) {
+hicache_path resolve_path(const Prepared& pr, Dir dir, int32_t layers) {
   if (pr.o.path != HICACHE_PATH_AUTO) return static_cast<hicache_path>(pr.o.path);
-  return choose_path(pr.pools, pr.o, pr.idx, dir);
+  return choose_path(pr.pools, pr.o, pr.idx, dir, layers);
 }
 
 void record_events(cudaEvent_t* evs, int32_t count, cudaStream_t stream) {
@@ -215,11 +215,13 @@ void record_events(cudaEvent_t* evs, int32_t count, cudaStream_t stream) {
 hicache_status load_layers(const Prepared& pr, int32_t layer_begin, int32_t layer_end,
                            cudaStream_t stream, cudaEvent_t* evs) {
   const int32_t count = layer_end - layer_begin;
-  const hicache_path path = resolve_path(pr, kPagedToDev);
+  const hicache_path path = resolve_path(pr, kPagedToDev, count);
   if (path == HICACHE_PATH_STAGED)
     return staged_load(pr.pools, pr.o, pr.idx, layer_begin, layer_end, stream, evs);
   const SideSpec side = host_side(pr.pools);
-  if (pr.o.burst_words && signaled_burst_available())
+  // one layer is one launch and its event either way: the signalling burst
+  // would only add its stream hand-offs
+  if (pr.o.burst_words && count > 1 && signaled_burst_available())
     return signaled_burst(pr.pools, side, pr.idx, pr.o, layer_begin, layer_end, stream, evs);
   const LaunchCfg cfg = launch_cfg(pr.o);
   for (int32_t l = layer_begin; l < layer_end; ++l) {
@@ -258,7 +260,7 @@ extern "C" hicache_status hicache_backup_all_layers(const hicache_pool* pools, i
   if (st != HICACHE_OK || n == 0) return st;
   st = stage_indices(&pr, stream);
   if (st != HICACHE_OK) return st;
-  const hicache_path path = resolve_path(pr, kDevToPaged);
+  const hicache_path path = resolve_path(pr, kDevToPaged, pr.pools[0].L);
   if (path == HICACHE_PATH_STAGED)
     return staged_backup(pr.pools, pr.o, pr.idx, stream);
   return launch_rows(pr.pools, host_side(pr.pools), pr.idx.dev_gpu, pr.idx.host_gpu, pr.idx.bits,
@@ -388,6 +390,38 @@ extern "C" hicache_status hicache_backup_all_layers_static_staging(
                /*dest_is_device=*/false, false, 0, 0, &pr);
   if (st != HICACHE_OK || n == 0) return st;
   return staged_backup(pr.pools, pr.o, pr.idx, stream);
+}
+
+extern "C" hicache_status hicache_auto_path(const hicache_pool* pools, int32_t num_pools,
+                                            const void* device_indices, const void* host_indices,
+                                            int32_t index_bits, int64_t n,
+                                            const hicache_opts* opts, int32_t op, int32_t layers,
+                                            int32_t* path_out) {
+  clear_error();
+  if (!path_out) return fail(HICACHE_EINVAL, "path_out is NULL");
+  if (op != HICACHE_OP_BACKUP && op != HICACHE_OP_LOAD)
+    return fail(HICACHE_EINVAL, "op must be HICACHE_OP_BACKUP or HICACHE_OP_LOAD");
+  std::vector<PoolInfo> checked;
+  hicache_status st = check_pools(pools, num_pools, &checked);
+  if (st != HICACHE_OK) return st;
+  const hicache_opts o = opts ? *opts : default_opts();
+  st = check_opts(o);
+  if (st == HICACHE_OK) st = check_index_args(device_indices, host_indices, index_bits, n);
+  if (st != HICACHE_OK) return st;
+  if (o.path != HICACHE_PATH_AUTO) {
+    *path_out = o.path;
+    return HICACHE_OK;
+  }
+  IndexSet idx;
+  idx.bits = index_bits;
+  idx.n = n;
+  if (o.index_location == HICACHE_INDEX_HOST) {
+    idx.dev_cpu = device_indices;
+    idx.host_cpu = host_indices;
+  }
+  *path_out = choose_path(checked, o, idx, op == HICACHE_OP_BACKUP ? kDevToPaged : kPagedToDev,
+                          op == HICACHE_OP_BACKUP ? checked[0].L : layers);
+  return HICACHE_OK;
 }
 
 extern "C" hicache_status hicache_plan_runs(const void* device_indices, const void* host_indices,

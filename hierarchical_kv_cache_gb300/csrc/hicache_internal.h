@@ -148,15 +148,18 @@ hicache_status plan_runs(const void* dev_idx, const void* host_idx, int32_t inde
 
 // Launch-side helpers (zero_copy.cu).
 // Default CTAs per SM of a copy launch (256 threads each).  Measured on GB300:
-// one CTA per SM already reaches the host-link peak in either direction alone.
-// When a backup and a load-back share the link, the device-to-host side does
-// best with one CTA per SM (more writes in flight slow the host reads) and the
-// host-to-device side with two, which brings both together to 92 % of the
-// bidirectional DMA peak.  The staged path's gather and scatter (between the
-// device pool and HBM staging, overlapped with copy-engine DMA) take two; with
-// four the staged backup measured slower (139 against 169 GB/s).
+// one CTA per SM reaches the host-link peak in either direction alone (two
+// per SM moved no more: 210.3 against 210.4 GB/s for a 32-layer burst).
+// Beside compute the count matters: with a bf16 GEMM loop running, a burst of
+// two CTAs per SM cost the GEMM 59-64 % of its throughput during the burst,
+// one per SM 27-34 %, at the same transfer speed.  Two per SM only pays when
+// a backup and a load-back share the link (duplex: 315 against 263 GB/s); a
+// caller that runs them concurrently can ask for it with opts.max_ctas.  The
+// staged path's gather and scatter row kernels (between the device pool and
+// HBM staging, overlapped with copy-engine DMA) take two; with four the
+// staged backup measured slower (139 against 169 GB/s).
 constexpr int kCtasPerSmToHost = 1;
-constexpr int kCtasPerSmFromHost = 2;
+constexpr int kCtasPerSmFromHost = 1;
 constexpr int kCtasPerSmHbm = 2;
 
 struct LaunchCfg {

@@ -470,19 +470,35 @@ hicache_status staged_load(const std::vector<PoolInfo>& all_pools, const hicache
 }
 
 hicache_path choose_path(const std::vector<PoolInfo>& pools, const hicache_opts& o,
-                         const IndexSet& idx, Dir dir) {
-  (void)pools;
-  (void)o;
-  (void)idx;
-  (void)dir;
-  // Measured on GB300 (NVLink-C2C host link) over row sizes 16..2048 B, page
-  // sizes 1..256, 1K..256K tokens, contiguous and fragmented pairs, both
-  // directions: the zero-copy kernel reaches the copy-engine bandwidth by
-  // itself and was at least as fast as the staged path at every point where
-  // both apply (the staged path pays an HBM round trip and one DMA call per
-  // host-page run).  AUTO therefore always takes the zero-copy path; the staged
-  // path stays available on request, e.g. to keep the SMs free for compute.
-  return HICACHE_PATH_ZERO_COPY;
+                         const IndexSet& idx, Dir dir, int32_t layers) {
+  // Measured on GB300 (NVLink-C2C host link): with the SMs to itself the
+  // zero-copy kernel reaches the copy-engine bandwidth and was at least as
+  // fast as the staged path at every point of the row size / page size /
+  // length sweep.  Its bandwidth grows with its CTAs, though, until about 38
+  // fill the link, while the staged path needs SMs only for short gather and
+  // scatter kernels.  So when the caller caps the copy's CTAs to keep the SMs
+  // for compute, below the crossover the staged path is faster, where it may
+  // run and its DMAs are large.
+  const int32_t below = dir == kDevToPaged ? HICACHE_AUTO_STAGED_BELOW_CTAS_BACKUP
+                                           : HICACHE_AUTO_STAGED_BELOW_CTAS_LOAD;
+  if (o.max_ctas <= 0 || o.max_ctas >= below) return HICACHE_PATH_ZERO_COPY;
+  if (dir == kPagedToDev && layers < 2) return HICACHE_PATH_ZERO_COPY;
+  if (!o.staging[0] || !o.staging[1] || o.staging_bytes == 0) return HICACHE_PATH_ZERO_COPY;
+  if (o.index_location != HICACHE_INDEX_HOST || !idx.host_cpu || idx.n == 0)
+    return HICACHE_PATH_ZERO_COPY;
+  int64_t largest = 0;
+  for (const PoolInfo& pi : pools)
+    largest = std::max(largest, int64_t(pi.L) * pi.P * pi.token_bytes);
+  if (largest < kDirectPageBytes) return HICACHE_PATH_ZERO_COPY;
+  std::vector<int64_t> hp;
+  if (!host_page_groups(idx.host_cpu, idx.bits, idx.n, pools[0].P, &hp))
+    return HICACHE_PATH_ZERO_COPY;
+  std::vector<size_t> staged_ids, direct_ids;
+  split_pools(pools, &staged_ids, &direct_ids);
+  const int32_t staged_layers = dir == kDevToPaged ? pools[0].L : 1;
+  if (layout_for(pick(pools, staged_ids), o, staged_layers).cap_pages < 1)
+    return HICACHE_PATH_ZERO_COPY;
+  return HICACHE_PATH_STAGED;
 }
 
 }  // namespace hk

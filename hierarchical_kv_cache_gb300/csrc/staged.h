@@ -25,9 +25,10 @@ hicache_status staged_load(const std::vector<PoolInfo>& pools, const hicache_opt
 // events the staged path uses (later calls find them ready).
 hicache_status staged_resources_ready();
 
-// AUTO path choice for one call.
+// AUTO path choice for one call that moves `layers` layers (see
+// hicache_auto_path in hicache.h for the rule).
 hicache_path choose_path(const std::vector<PoolInfo>& pools, const hicache_opts& o,
-                         const IndexSet& idx, Dir dir);
+                         const IndexSet& idx, Dir dir, int32_t layers);
 
 // Host page of each group of page_size pairs when the pairs are whole aligned
 // host pages in groups (pairs kP..kP+P-1 are host tokens p*P..p*P+P-1);

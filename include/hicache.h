@@ -75,7 +75,7 @@
 extern "C" {
 #endif
 
-#define HICACHE_ABI_VERSION 4 /* 4: adds hicache_check_pairs */
+#define HICACHE_ABI_VERSION 5 /* 5: adds hicache_auto_path; 4: adds hicache_check_pairs */
 
 typedef enum hicache_status {
   HICACHE_OK = 0,
@@ -90,7 +90,7 @@ typedef enum hicache_status {
 } hicache_status;
 
 typedef enum hicache_path {
-  HICACHE_PATH_AUTO = 0,      /* the library chooses per call from row size, run length, direction */
+  HICACHE_PATH_AUTO = 0,      /* the library chooses per call (hicache_auto_path gives the rule) */
   HICACHE_PATH_ZERO_COPY = 1, /* SMs read and write the mapped pinned host pool directly */
   HICACHE_PATH_STAGED = 2     /* gather/scatter through HBM staging + copy-engine DMA */
 } hicache_path;
@@ -145,8 +145,13 @@ typedef struct hicache_pool {
 typedef struct hicache_opts {
   int32_t path;            /* hicache_path */
   int32_t index_location;  /* hicache_index_location */
-  int32_t max_ctas;        /* 0 = library default; else caps the CTAs of each copy kernel so that
-                              a concurrent consumer keeps the remaining SMs */
+  int32_t max_ctas;        /* 0 = library default (one 256-thread CTA per SM for the host-link
+                              copies); else caps the CTAs of each copy kernel, so that compute
+                              running at the same time keeps the other SMs.  Measured on GB300
+                              beside a bf16 GEMM loop: 38 CTAs still moved 142-171 GB/s and cost
+                              the GEMM 6-17 % of its throughput, against 27-34 % with the
+                              default.  Below HICACHE_AUTO_STAGED_BELOW_CTAS_* the AUTO path may
+                              switch to the staged path (see hicache_auto_path). */
   int32_t reserved;        /* must be 0 */
   void* staging[2];        /* staged path: two device buffers used alternately, 16-byte aligned */
   size_t staging_bytes;    /* bytes of each staging buffer */
@@ -276,6 +281,47 @@ hicache_status hicache_backup_all_layers_static_staging(const hicache_pool* pool
                                                         int32_t index_bits, int64_t n,
                                                         const hicache_opts* opts,
                                                         cudaStream_t stream);
+
+/* Operations, for hicache_auto_path. */
+#define HICACHE_OP_BACKUP 0 /* hicache_backup_all_layers */
+#define HICACHE_OP_LOAD 1   /* hicache_load_layer (1 layer) or hicache_load_burst */
+
+/* Copy-CTA budgets (opts->max_ctas) below which HICACHE_PATH_AUTO takes the
+ * staged path when it may (see hicache_auto_path), per direction. */
+#define HICACHE_AUTO_STAGED_BELOW_CTAS_BACKUP 24
+#define HICACHE_AUTO_STAGED_BELOW_CTAS_LOAD 32
+
+/*
+ * The path a call with opts->path == HICACHE_PATH_AUTO takes (host only; no
+ * CUDA call, so a scheduler may ask ahead of the call).  Writes
+ * HICACHE_PATH_ZERO_COPY or HICACHE_PATH_STAGED to *path_out.
+ *   op     : HICACHE_OP_BACKUP or HICACHE_OP_LOAD.
+ *   layers : for a load, the layers the call moves (1 for hicache_load_layer,
+ *            layer_end - layer_begin for a burst); ignored for a backup.
+ *   Index arrays are read only when opts->index_location is HICACHE_INDEX_HOST
+ *   (then they must be host memory); n pairs of index_bits bits.
+ * The rule, from measurements on GB300 (zero-copy bandwidth grows with its
+ * CTAs until about 38 of them fill the host link; the staged path moves its
+ * bytes with the copy engine and needs SMs only for short gather and scatter
+ * kernels):
+ *   the staged path when all of these hold, else zero-copy:
+ *   - opts->max_ctas is set (the caller keeps the other SMs for compute) and
+ *     below HICACHE_AUTO_STAGED_BELOW_CTAS_BACKUP / _LOAD;
+ *   - two staging buffers are given, holding at least one host page of every
+ *     staged pool (of all layers for a backup, of one layer for a load);
+ *   - host-located indices whose pairs are whole host pages;
+ *   - the largest pool's host page (all layers of one tensor) is at least
+ *     1 MiB, so that one DMA per page is not dominated by the copy engine's
+ *     fixed cost per copy;
+ *   - for a load, at least two layers (a single layer would be one small DMA
+ *     per page).
+ * Errors: the argument checks of the calls (pools, opts, index arguments),
+ * HICACHE_EINVAL for a bad op or a NULL path_out.
+ */
+hicache_status hicache_auto_path(const hicache_pool* pools, int32_t num_pools,
+                                 const void* device_indices, const void* host_indices,
+                                 int32_t index_bits, int64_t n, const hicache_opts* opts,
+                                 int32_t op, int32_t layers, int32_t* path_out);
 
 /* Bytes of opts->index_staging that a call with n pairs of index_bits-bit
  * indices needs (both arrays, each 16-byte aligned). */

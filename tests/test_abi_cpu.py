@@ -36,7 +36,7 @@ def test_header_symbols_exported():
     lib = ctypes.CDLL(B.LIB_PATH)
     missing = [n for n in names if not hasattr(lib, n)]
     assert not missing, f"declared but not exported: {missing}"
-    assert hk.abi_version() == 4
+    assert hk.abi_version() == 5
 
 
 def brute_runs(d, h, P):
@@ -246,4 +246,4 @@ def test_concurrent_builds_compile_once(tmp_path):
             if f.endswith(".o")]
     assert objs and all(os.path.getmtime(o) <= mtime for o in objs)
     lib = ctypes.CDLL(B.LIB_PATH)
-    assert lib.hicache_abi_version() == 4
+    assert lib.hicache_abi_version() == 5

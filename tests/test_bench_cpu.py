@@ -51,7 +51,14 @@ def test_traffic_record_matches_the_kernel_source():
     sys.path.insert(0, REPO)
     import bench
 
-    for which in ("backup_all_layers", "load_one_layer", "load_burst_signalling"):
-        t = bench.traffic_per_launch(which, 1 << 30)
-        assert t is not None, f"{which}: the record does not match csrc/row_copy_kernel.cuh"
-        assert (1 << 30) * 0.95 < t < (1 << 30) * 1.05 or which != "backup_all_layers"
+    for workload, whiches in (("mla78_dsa", ("backup_all_layers", "load_burst_signalling")),
+                              ("llama3_8b_mha", ("backup_all_layers", "load_one_layer",
+                                                 "load_burst_signalling"))):
+        for which in whiches:
+            t = bench.traffic_per_launch(workload, which, 1 << 30)
+            assert t is not None, \
+                f"{workload} {which}: the record does not match csrc/row_copy_kernel.cuh"
+            assert (1 << 30) * 0.95 < t < (1 << 30) * 1.05 or which != "backup_all_layers"
+    # a launch or workload the record does not hold has no traffic figure
+    assert bench.traffic_per_launch("mla78_dsa", "load_one_layer", 1 << 30) is None
+    assert bench.traffic_per_launch("mla78_dsa:page_first", "backup_all_layers", 1 << 30) is None
