@@ -1180,13 +1180,17 @@ def run_latency(args, reps=30):
     stream, so that the timing events around it hold its GPU work only, not the
     host's enqueue (median of `reps`).  call-to-done: wall time from the call on
     an idle stream to the end of a synchronize, what a caller waiting for the
-    op sees.  host enqueue: the call's own host time.  Ops: the all-layer
+    op sees.  host enqueue: the Python call's host time; library host: the same
+    call through the C ABI with its arguments built beforehand.  Ops: the all-layer
     backup, one layer's load, and the whole load-back burst (single-launch, one
     event per layer), with device-located indices, on the first k pages of the
     workload's lists.
     """
+    import ctypes
+
     import torch
     import hierarchical_kv_cache_gb300 as hk
+    from hierarchical_kv_cache_gb300 import _binding as B
     from hierarchical_kv_cache_gb300 import pools as hpools
     from hierarchical_kv_cache_gb300.build import build
 
@@ -1218,12 +1222,31 @@ def run_latency(args, reps=30):
                    pools, 0, ht, d2t, opts=opts, stream=stream, layer_done=evs[0])),
                "load_burst": (bytes_layer * L, lambda: hk.hicache_load_burst(
                    pools, 0, L, ht, d2t, opts=opts, stream=stream, layer_done=evs))}
+        # the same calls through the C ABI with every argument built beforehand:
+        # the library's own host time, without the Python binding's marshalling
+        lib = hk.lib()
+        arr, npools, keep = B._pools_arg(pools)
+        co = B._opts_arg(opts, dt, ht)
+        sh = stream.cuda_stream
+        ev_h = (ctypes.c_void_p * L)(*[B._event_handle(e, sh) for e in evs])
+        raw = {"backup_all_layers": lambda: lib.hicache_backup_all_layers(
+                   arr, npools, dt.data_ptr(), ht.data_ptr(), 64, m, ctypes.byref(co), sh),
+               "load_one_layer": lambda: lib.hicache_load_layer(
+                   arr, npools, 0, ht.data_ptr(), d2t.data_ptr(), 64, m, ctypes.byref(co), sh,
+                   ev_h[0]),
+               "load_burst": lambda: lib.hicache_load_burst(
+                   arr, npools, 0, L, ht.data_ptr(), d2t.data_ptr(), 64, m, ctypes.byref(co), sh,
+                   ev_h)}
         for name, (nbytes, fn) in ops.items():
             for _ in range(3):
                 fn()
             torch.cuda.synchronize()
-            dev_us, wall_us, enq_us = [], [], []
+            dev_us, wall_us, enq_us, lib_us = [], [], [], []
             for _ in range(reps):
+                stream.synchronize()
+                w0 = time.perf_counter()
+                assert raw[name]() == hk.HICACHE_OK
+                lib_us.append((time.perf_counter() - w0) * 1e6)
                 t0 = torch.cuda.Event(enable_timing=True)
                 t1 = torch.cuda.Event(enable_timing=True)
                 stream.synchronize()
@@ -1246,6 +1269,7 @@ def run_latency(args, reps=30):
                    "device_us_p50": round(med, 2), "device_us_min": round(min(dev_us), 2),
                    "call_to_done_us_p50": round(statistics.median(wall_us), 2),
                    "host_enqueue_us_p50": round(statistics.median(enq_us), 2),
+                   "library_host_us_p50": round(statistics.median(lib_us), 2),
                    "gbs": round(nbytes / (med * 1e-6) / GB, 2)}
             out.append(rec)
             print(json.dumps(rec), flush=True)

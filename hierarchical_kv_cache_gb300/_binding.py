@@ -141,13 +141,22 @@ class Pool:
     def to_c(self):
         """(c_pool, keep): the struct and the pointer arrays it points into.
 
-        The caller holds `keep` until the C call returns; nothing is stored on the
-        Pool, so threads may share one Pool.
+        The caller holds `keep` until the C call returns.  The last struct built
+        is kept on the Pool and reused while every buffer address and shape
+        field is unchanged (building the ctypes arrays costs tens of
+        microseconds for a pool of many layers); threads may share one Pool.
         """
         T, L = self.num_tensors, self.num_layers
-        dev = (ctypes.c_void_p * (T * L))(*[self.device_layers[t][l].data_ptr()
-                                            for t in range(T) for l in range(L)])
-        host = (ctypes.c_void_p * T)(*[h.data_ptr() for h in self.host_tensors])
+        dev_ptrs = [self.device_layers[t][l].data_ptr() for t in range(T) for l in range(L)]
+        host_ptrs = [h.data_ptr() for h in self.host_tensors]
+        key = (T, L, self.head_num, self.head_dim, self.dtype_size, self.page_size,
+               self.device_slots, self.host_pages, bool(self.page_granular), int(self.layout),
+               tuple(dev_ptrs), tuple(host_ptrs))
+        cached = self.__dict__.get("_c_cache")
+        if cached is not None and cached[0] == key:
+            return cached[1], cached[2]
+        dev = (ctypes.c_void_p * (T * L))(*dev_ptrs)
+        host = (ctypes.c_void_p * T)(*host_ptrs)
         st = c_pool(num_layers=L, num_tensors=T, head_num=self.head_num,
                     head_dim=self.head_dim, dtype_size=self.dtype_size,
                     page_size=self.page_size, page_granular=int(self.page_granular),
@@ -155,6 +164,7 @@ class Pool:
                     host_pages=self.host_pages,
                     device_layers=ctypes.cast(dev, ctypes.POINTER(ctypes.c_void_p)),
                     host_tensors=ctypes.cast(host, ctypes.POINTER(ctypes.c_void_p)))
+        self.__dict__["_c_cache"] = (key, st, (dev, host))
         return st, (dev, host)
 
 

@@ -17,6 +17,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -145,22 +146,30 @@ hicache_status signaled_burst(const std::vector<PoolInfo>& pools, const SideSpec
     record_from(evs, first, count, stream);
     return st;
   }
+  // one wait per group of layers holding kSignalGroupBytes (one per layer for
+  // layers that large): the flag of the group's last layer covers the group
+  const int32_t per_group = int32_t(std::max<int64_t>(
+      1, std::min<int64_t>(count, (kSignalGroupBytes + layer_bytes - 1) / std::max<int64_t>(1, layer_bytes))));
   int32_t i = first;
-  for (; i < count; ++i) {
+  while (i < count) {
+    const int32_t last = std::min(count, i + per_group) - 1;
     const CUresult cr = wait(reinterpret_cast<CUstream>(r->sig),
-                             reinterpret_cast<CUdeviceptr>(bw.flag + (i - first)), 1u,
+                             reinterpret_cast<CUdeviceptr>(bw.flag + (last - first)), 1u,
                              CU_STREAM_WAIT_VALUE_GEQ);
     if (cr != CUDA_SUCCESS) {
       st = fail(HICACHE_ECUDA, "cuStreamWaitValue32 failed with CUresult " + std::to_string(int(cr)));
       break;
     }
-    if (evs && evs[i]) {
-      e = cudaEventRecord(evs[i], r->sig);
-      if (e != cudaSuccess) {
-        st = cuda_fail(e, "cudaEventRecord(layer_done)");
-        break;  // evs[i] is recorded on the caller's stream below
+    for (; i <= last; ++i) {
+      if (evs && evs[i]) {
+        e = cudaEventRecord(evs[i], r->sig);
+        if (e != cudaSuccess) {
+          st = cuda_fail(e, "cudaEventRecord(layer_done)");
+          break;  // evs[i] is recorded on the caller's stream below
+        }
       }
     }
+    if (st != HICACHE_OK) break;
   }
   // layers whose wait could not be enqueued complete after the launch, on the caller's stream
   record_from(evs, i, count, stream);

@@ -78,8 +78,9 @@ struct Segment {
 // ordered layer-major, segs_per_layer per layer; layer k of the launch is
 // burst layer layer_base + k.  Words (device memory, zeroed before the launch):
 // done[burst layer] counts finished tasks, flag[burst layer] becomes 1 once
-// every task of that layer has landed; exits[launch first layer] counts CTAs
-// that left the launch and next[launch first layer] hands out its tasks.
+// every task of that layer and of every earlier layer of the burst has landed
+// (so one flag covers a group of layers); exits[launch first layer] counts
+// CTAs that left the launch and next[launch first layer] hands out its tasks.
 struct SignalSpec {
   uint32_t* done = nullptr;
   uint32_t* flag = nullptr;

@@ -33,8 +33,33 @@ __device__ __forceinline__ uint32_t ld_stream(const uint32_t* p) { return __ldcs
 __device__ __forceinline__ void st_stream(uint4* p, const uint4& v) { __stcs(p, v); }
 __device__ __forceinline__ void st_stream(uint32_t* p, const uint32_t& v) { __stcs(p, v); }
 
+// Burst-relative layer l has just completed.  Publishes its flag and the flags
+// of the complete layers after it, as long as every earlier layer is
+// published, so that flag[l] set means layers 0..l of the burst's signalled
+// range have all landed: a stream wait on one flag covers a whole group of
+// layers.  A completion that finds the layer before it unpublished stops
+// there; the warp that publishes that layer then finds this one complete and
+// carries on.  Both sides write (their done count, or a flag), fence and then
+// read the other side's word, so at least one of them sees the other's write
+// (publishing twice is harmless).  Called by one lane.
+template <int MAXSEG>
+__device__ __forceinline__ void publish_from(const CopyParams<MAXSEG>& p, int l) {
+  const int end = p.sig.layer_base + p.sig.nlayers;
+  for (;;) {
+    __threadfence();
+    if (l > 0 && *reinterpret_cast<volatile const uint32_t*>(&p.sig.flag[l - 1]) == 0) return;
+    atomicExch(&p.sig.flag[l], 1u);
+    __threadfence();
+    if (++l >= end) return;
+    if (int64_t(*reinterpret_cast<volatile const uint32_t*>(&p.sig.done[l])) !=
+        p.sig.tasks_per_layer)
+      return;
+  }
+}
+
 // Adds `count` finished tasks to burst layer `layer`; the warp that completes
-// the layer publishes its flag.  Called by all 32 lanes of a warp.
+// the layer publishes its flag (and those after it, see publish_from).  Called
+// by all 32 lanes of a warp.
 template <int MAXSEG>
 __device__ __forceinline__ void flush_layer(const CopyParams<MAXSEG>& p, int layer,
                                             uint32_t count, int lane) {
@@ -43,10 +68,7 @@ __device__ __forceinline__ void flush_layer(const CopyParams<MAXSEG>& p, int lay
   if (lane == 0) {
     const int l = p.sig.layer_base + layer;
     const uint32_t before = atomicAdd(&p.sig.done[l], count);
-    if (int64_t(before) + count == p.sig.tasks_per_layer) {
-      __threadfence();
-      atomicExch(&p.sig.flag[l], 1u);
-    }
+    if (int64_t(before) + count == p.sig.tasks_per_layer) publish_from(p, l);
   }
 }
 

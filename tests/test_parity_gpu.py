@@ -945,17 +945,21 @@ def test_empty_lists_record_events_and_move_nothing():
 
 # ----------------------------------------------------- events gate a consumer
 
+@pytest.mark.parametrize("pages", [256, 8])
 @pytest.mark.parametrize("burst", BURSTS + ["staged"])
-def test_layer_events_gate_consumer_checksum(burst):
+def test_layer_events_gate_consumer_checksum(burst, pages):
     """A consumer on another stream waits on event l only, and must see layer l fully loaded.
 
-    The staged variant has room for 4 layers of every page, so its layers land
-    in groups of 1, 2, 4 and 5, the last in chunks of 204 and 52 pages.
+    With 256 pages a layer holds 18.9 MB: the single-launch burst waits for each
+    layer's word.  With 8 pages a layer holds 590 KB, so that burst waits once
+    per group of 4 layers and records the group's events together; each event
+    must still gate its own layer.  The staged variant has room for 4 layers of
+    every page, so its layers land in groups.
     """
     s = G.shape("mla", L=12, T=1, head_num=1, head_dim=576, dtype_size=2, P=64, slots=65536,
                 pages=512)
     pool = G.make_pool(s, 20)
-    d, h, _, _ = W.page_pairs(21, 256, s.device_slots // 64, s.host_pages, 64)
+    d, h, _, _ = W.page_pairs(21, pages, s.device_slots // 64, s.host_pages, 64)
     host0 = G.host_images(pool)
     dt, ht = G.index_tensors(d, h, "device")
     events = [torch.cuda.Event() for _ in range(s.num_layers)]
