@@ -598,6 +598,7 @@ def run_ours(args, rank, world):
             "first_event_within_bound": first_us <= bound_us,
             "step_ms_min_median_max": [round(min(t_step), 4), round(statistics.median(t_step), 4),
                                        round(max(t_step), 4)],
+            "step_ms_each": [round(t, 3) for t in t_step],
             "backup_ms_p50": round(statistics.median(t_backup), 4),
             "load_burst_ms_p50": round(statistics.median(t_load), 4),
             "layer_event_us_median_step": [round(ev_m[k_med].elapsed_time(e) * 1e3, 1)

@@ -255,7 +255,7 @@ __global__ void __launch_bounds__(32) page_block_kernel(const __grid_constant__ 
           // Give up: report, let the loads still in flight land (bounded),
           // and let every store finish before the shared memory goes away.
           if (p.err) atomicOr(p.err, HICACHE_DEVERR_TIMEOUT);
-          for (int64_t j = k + 1; j < issued; ++j)
+          for (int64_t j = k; j < issued; ++j)  // this item's load too
             mbar_wait(&bar[j % kStages], uint32_t((j / kStages) & 1));
           gave_up = true;
           break;
