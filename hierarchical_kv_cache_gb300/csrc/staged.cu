@@ -36,7 +36,8 @@ hicache_status cuda_fail(cudaError_t e, const std::string& what) {
 struct StagedRes {
   bool init = false;
   cudaStream_t copy = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr;
+  cudaStream_t side = nullptr;  // zero-copy share of a staged backup
+  cudaEvent_t fork = nullptr, join = nullptr, side_done = nullptr;
   cudaEvent_t ready[2] = {nullptr, nullptr};
   cudaEvent_t freed[2] = {nullptr, nullptr};
 };
@@ -49,7 +50,9 @@ hicache_status get_res(StagedRes** out) {
   StagedRes& r = res[dev];
   if (!r.init) {
     HK_CUDA(cudaStreamCreateWithFlags(&r.copy, cudaStreamNonBlocking), "cudaStreamCreate(copy)");
-    cudaEvent_t* evs[6] = {&r.fork, &r.join, &r.ready[0], &r.ready[1], &r.freed[0], &r.freed[1]};
+    HK_CUDA(cudaStreamCreateWithFlags(&r.side, cudaStreamNonBlocking), "cudaStreamCreate(side)");
+    cudaEvent_t* evs[7] = {&r.fork,     &r.join,     &r.side_done, &r.ready[0],
+                           &r.ready[1], &r.freed[0], &r.freed[1]};
     for (cudaEvent_t* e : evs) HK_CUDA(cudaEventCreateWithFlags(e, cudaEventDisableTiming), "cudaEventCreate");
     r.init = true;
   }
@@ -167,6 +170,13 @@ bool device_pages_consecutive(const void* dev_idx, int32_t bits, int64_t n, int3
 // 659 KB per page) is such a pool beside its 5.75 MB latent pages.
 constexpr int64_t kDirectPageBytes = int64_t(1) << 20;
 
+// A staged call moves this fraction of its work (1 / kZeroCopyShare) zero-copy
+// beside the copy engine: the last pages of a backup, the first layers of a
+// load.  The copy engine leaves the link idle for its fixed time per copy
+// (2.4-3.3 us on GB300) and moves a load's first small layer groups at a
+// fraction of the link; SM-issued traffic beside it fills those gaps.
+constexpr int64_t kZeroCopyShare = 8;
+
 // Splits a staged call's pools into those that go through staging and the
 // small ones that move zero-copy beside them.
 void split_pools(const std::vector<PoolInfo>& pools, std::vector<size_t>* staged,
@@ -246,42 +256,57 @@ hicache_status staged_backup(const std::vector<PoolInfo>& all_pools, const hicac
   if (st != HICACHE_OK) return st;
   cudaStream_t copy = o.copy_stream ? o.copy_stream : r->copy;
   const LaunchCfg cfg{o.max_ctas, o.device_error, /*paged_in_hbm=*/true};
+  const LaunchCfg zero_copy{o.max_ctas, o.device_error, /*paged_in_hbm=*/false};
   const int64_t groups = int64_t(hp.size());
+  // the last pages move zero-copy beside the copy engine (kZeroCopyShare)
+  const int64_t zc_pages = groups >= kZeroCopyShare ? (groups + kZeroCopyShare - 1) / kZeroCopyShare : 0;
+  const int64_t dma_groups = groups - zc_pages;
   const bool dev_consecutive = device_pages_consecutive(idx.dev_cpu, idx.bits, idx.n, P);
   const SideSpec side[2] = {staging_side(pools, lay, static_cast<char*>(o.staging[0]), L, 0),
                             staging_side(pools, lay, static_cast<char*>(o.staging[1]), L, 0)};
+  const bool use_side = zc_pages > 0 || !direct.empty();
 
   HK_CUDA(cudaEventRecord(r->fork, stream), "cudaEventRecord(fork)");
   HK_CUDA(cudaStreamWaitEvent(copy, r->fork, 0), "cudaStreamWaitEvent(fork)");
-  // From here on every return joins the copy stream back into `stream`, also
-  // on failure: copies of earlier chunks may still be in flight, and the next
-  // call ordered on `stream` may reuse the staging buffers they read.
+  if (use_side) HK_CUDA(cudaStreamWaitEvent(r->side, r->fork, 0), "cudaStreamWaitEvent(fork)");
+  // From here on every return joins the copy stream (and the side stream)
+  // back into `stream`, also on failure: copies of earlier chunks may still be
+  // in flight, and the next call ordered on `stream` may reuse the staging
+  // buffers they read.
   auto join = [&](hicache_status s) {
     cudaError_t e = cudaEventRecord(r->join, copy);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, r->join, 0);
+    if (e == cudaSuccess && use_side) e = cudaEventRecord(r->side_done, r->side);
+    if (e == cudaSuccess && use_side) e = cudaStreamWaitEvent(stream, r->side_done, 0);
     if (e != cudaSuccess && s == HICACHE_OK) s = cuda_fail(e, "staged backup join");
     return s;
   };
+  // The zero-copy share on the side stream, concurrent with the gathers and
+  // DMAs: every pool's last zc_pages pages and every page of the small pools.
+  if (zc_pages > 0) {
+    st = launch_rows(pools, host_side(pools), idx.dev_gpu, idx.host_gpu, idx.bits,
+                     dma_groups * P, zc_pages * P, kDevToPaged, 0, L, zero_copy, r->side);
+    if (st != HICACHE_OK) return join(st);
+  }
+  if (!direct.empty()) {
+    st = launch_rows(direct, host_side(direct), idx.dev_gpu, idx.host_gpu, idx.bits, 0, idx.n,
+                     kDevToPaged, 0, L, zero_copy, r->side);
+    if (st != HICACHE_OK) return join(st);
+  }
 #define HK_TRY(call, what)                                  \
   do {                                                      \
     const cudaError_t e_ = (call);                          \
     if (e_ != cudaSuccess) return join(cuda_fail(e_, what)); \
   } while (0)
-  for (int64_t k = 0, g0 = 0; g0 < groups; ++k, g0 += lay.cap_pages) {
+  for (int64_t k = 0, g0 = 0; g0 < dma_groups; ++k, g0 += lay.cap_pages) {
     const int b = int(k & 1);
-    const int64_t g1 = std::min(groups, g0 + lay.cap_pages);
+    const int64_t g1 = std::min(dma_groups, g0 + lay.cap_pages);
     // the DMA of chunk k-2 must have drained buffer b before the gather reuses it
     if (k >= 2) HK_TRY(cudaStreamWaitEvent(stream, r->freed[b], 0), "cudaStreamWaitEvent(freed)");
     st = move_staging(pools, side[b], idx, dev_consecutive, g0, g1, kDevToPaged, 0, L, cfg, stream);
     if (st != HICACHE_OK) return join(st);
     HK_TRY(cudaEventRecord(r->ready[b], stream), "cudaEventRecord(ready)");
     HK_TRY(cudaStreamWaitEvent(copy, r->ready[b], 0), "cudaStreamWaitEvent(ready)");
-    if (k == 0 && !direct.empty()) {
-      // the small pools, zero-copy, while the copy engine drains the first chunk
-      st = launch_rows(direct, host_side(direct), idx.dev_gpu, idx.host_gpu, idx.bits, 0, idx.n,
-                       kDevToPaged, 0, L, LaunchCfg{o.max_ctas, o.device_error}, stream);
-      if (st != HICACHE_OK) return join(st);
-    }
     for (size_t p = 0; p < pools.size(); ++p) {
       const PoolInfo& pi = pools[p];
       const int64_t page_bytes = int64_t(L) * pi.P * pi.token_bytes;  // one host page, all layers
@@ -308,11 +333,12 @@ hicache_status staged_backup(const std::vector<PoolInfo>& all_pools, const hicac
 // one 64-token page of 2 KiB rows) moves 33 GB/s, a 512 KiB copy 106 GB/s,
 // 2 MiB 170 GB/s and 4 MiB 186 GB/s (host to device).  The staged load
 // therefore copies a group of consecutive layers of each host page per DMA
-// (they are adjacent in a page-first host page).  The groups grow fourfold,
-// 4, 16, ... layers after the first layer (read zero-copy), until one copy
-// carries about this many bytes; a tail shorter than its group is merged or
-// split evenly.  A 32-layer burst of 128 KiB blocks runs as 1, 4 and 27
-// layers, a 78-layer burst of 72 KiB blocks as 1, 4, 16, 29 and 28.
+// (they are adjacent in a page-first host page).  After the zero-copy first
+// layers the groups grow fourfold, 4, 16, ... layers, until one copy carries
+// about this many bytes; a tail shorter than its group is merged or split
+// evenly.  A 32-layer burst of 128 KiB blocks runs as 4 zero-copy layers, then
+// groups of 4 and 24; a 78-layer burst of 72 KiB blocks as 10 zero-copy
+// layers, then 4, 16 and 48.
 constexpr int64_t kDmaCopyTargetBytes = int64_t(4) << 20;
 constexpr int32_t kGroupGrowth = 4;
 // A group too large for the staging to hold every page at once moves in
@@ -372,23 +398,41 @@ hicache_status staged_load(const std::vector<PoolInfo>& all_pools, const hicache
     if (e_ != cudaSuccess) return finish(cuda_fail(e_, what)); \
   } while (0)
 
+  // The first layers of a burst of two or more (one in kZeroCopyShare, at
+  // least one) are read zero-copy: the SMs read the host pool directly, one
+  // launch and event per layer.  Through the copy engine the first layer
+  // would cost one small copy per host page before its event, and the first
+  // layer groups would move in copies too small for the link.  The copy stream
+  // forks once the first layer's launch is enqueued, so that layer has the
+  // link to itself; the other zero-copy layers share it with the copy
+  // engine's first, smaller groups, whose copies leave the link idle for part
+  // of their time.
+  const int32_t zc_layers =
+      count >= 2 ? int32_t(std::max<int64_t>(1, (count + kZeroCopyShare - 1) / kZeroCopyShare)) : 0;
+  auto load_direct_layer = [&](int32_t k) {
+    const hicache_status s = launch_rows(all_pools, host_side(all_pools), idx.dev_gpu,
+                                         idx.host_gpu, idx.bits, 0, idx.n, kPagedToDev, k, k + 1,
+                                         zero_copy, stream);
+    if (s != HICACHE_OK) return s;
+    if (layer_done && layer_done[k - layer_begin]) {
+      const cudaError_t e = cudaEventRecord(layer_done[k - layer_begin], stream);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(layer_done)");
+    }
+    ++recorded;
+    return HICACHE_OK;
+  };
+  if (zc_layers > 0) {
+    st = load_direct_layer(layer_begin);
+    if (st != HICACHE_OK) return finish(st);
+  }
   HK_TRY(cudaEventRecord(r->fork, stream), "cudaEventRecord(fork)");
   HK_TRY(cudaStreamWaitEvent(copy, r->fork, 0), "cudaStreamWaitEvent(fork)");
   forked = copy;
-  int32_t first = layer_begin;
-  if (count >= 2) {
-    // The first layer of a burst is latency-critical, and through the copy
-    // engine it would cost one small copy per host page before its event.  It
-    // is read zero-copy instead (the SMs read the host pool directly), while
-    // the copy stream already moves the next group.
-    st = launch_rows(all_pools, host_side(all_pools), idx.dev_gpu, idx.host_gpu, idx.bits, 0,
-                     idx.n, kPagedToDev, layer_begin, layer_begin + 1, zero_copy, stream);
+  for (int32_t k = layer_begin + 1; k < layer_begin + zc_layers; ++k) {
+    st = load_direct_layer(k);
     if (st != HICACHE_OK) return finish(st);
-    if (layer_done && layer_done[0])
-      HK_TRY(cudaEventRecord(layer_done[0], stream), "cudaEventRecord(layer_done)");
-    recorded = 1;
-    first = layer_begin + 1;
   }
+  const int32_t first = layer_begin + zc_layers;
   // The small pools' share of a scatter step: zero-copy from the host pool.
   auto move_direct = [&](int64_t g0, int64_t g1, int32_t l0, int32_t l1) {
     if (direct.empty()) return HICACHE_OK;
@@ -396,6 +440,8 @@ hicache_status staged_load(const std::vector<PoolInfo>& all_pools, const hicache
                        (g1 - g0) * P, kPagedToDev, l0, l1, zero_copy, stream);
   };
   int64_t step = 0;
+  // the groups start small whatever the zero-copy share, so that the layer
+  // events keep arriving in steps (a consumer starts on them early)
   int32_t g_want = first == layer_begin ? 1 : std::min(g_cap, kGroupGrowth);
   for (int32_t l = first, g = 1; l < layer_end; l += g) {
     // the next group size; a tail shorter than the group joins it (or, when

@@ -48,10 +48,11 @@
  *   before anything enqueued on `stream` after the call returns.  Index arrays,
  *   pools and staging buffers must stay valid until `stream` has passed the
  *   call.  Calls that share a staging buffer must be ordered by the caller.
- *   On first use on a thread and device, the staged path and the single-launch
- *   burst create one library stream and a few events there, kept until the
- *   process exits; bursts issued from one thread share that stream, so their
- *   layer events are recorded in issue order.
+ *   On first use on a thread and device, the single-launch burst creates one
+ *   library stream and the staged path two (copy engine and zero-copy share),
+ *   with a few events, kept until the process exits; bursts issued from one
+ *   thread share that stream, so their layer events are recorded in issue
+ *   order.
  *
  * Errors:
  *   Every function returns a hicache_status and never aborts or throws across
@@ -224,13 +225,17 @@ hicache_status hicache_load_layer(const hicache_pool* pools, int32_t num_pools, 
  * smaller layers are waited for in groups of about 2 MiB, whose events are
  * recorded together once the group's last layer has landed.  The words must not be shared by bursts that overlap on the
  * GPU.  The staged path ignores burst_words.
- * The staged path reads the first layer of a burst of two or more layers
- * zero-copy (the SMs read the host pool), then copies groups of consecutive
- * layers of each host page per DMA, groups of 2, 4, ... layers (up to about
- * 4 MiB per copy, in chunks of pages that fit a staging buffer), and scatters
- * and records the events of a group's layers one by one.  Its later layer
- * events therefore arrive in groups, each no earlier than its own layer's
- * data.
+ * The staged path reads the first layers of a burst of two or more layers
+ * zero-copy (the SMs read the host pool; one layer in eight, at least one,
+ * each with its own launch and event), then copies groups of consecutive
+ * layers of each host page per DMA, each group four times the previous (up to
+ * about 4 MiB per copy, in chunks of pages that fit a staging buffer), and
+ * scatters and records the events of a group's layers one by one.  Its later
+ * layer events therefore arrive in groups, each no earlier than its own
+ * layer's data.  A pool whose host page is under 1 MiB beside a larger pool
+ * moves zero-copy throughout.  The staged backup likewise moves the last
+ * eighth of its pages, and such small pools, zero-copy on a library stream
+ * beside its DMAs.
  */
 hicache_status hicache_load_burst(const hicache_pool* pools, int32_t num_pools,
                                   int32_t layer_begin, int32_t layer_end,
@@ -290,7 +295,7 @@ hicache_status hicache_backup_all_layers_static_staging(const hicache_pool* pool
 
 /* Copy-CTA budgets (opts->max_ctas) below which HICACHE_PATH_AUTO takes the
  * staged path when it may (see hicache_auto_path), per direction. */
-#define HICACHE_AUTO_STAGED_BELOW_CTAS_BACKUP 24
+#define HICACHE_AUTO_STAGED_BELOW_CTAS_BACKUP 32
 #define HICACHE_AUTO_STAGED_BELOW_CTAS_LOAD 32
 
 /*

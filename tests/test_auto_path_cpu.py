@@ -194,3 +194,16 @@ class _Numel(_Addr):
 
     def element_size(self):
         return 1
+
+
+def test_binding_constants_match_the_header():
+    import os
+    import re
+
+    text = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                             "include", "hicache.h")).read()
+    for name in ("HICACHE_AUTO_STAGED_BELOW_CTAS_BACKUP", "HICACHE_AUTO_STAGED_BELOW_CTAS_LOAD",
+                 "HICACHE_OP_BACKUP", "HICACHE_OP_LOAD", "HICACHE_DEVERR_TIMEOUT"):
+        m = re.search(r"#define\s+%s\s+(\d+)" % name, text)
+        assert m, name
+        assert int(m.group(1)) == getattr(hk, name), name
