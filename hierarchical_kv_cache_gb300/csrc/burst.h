@@ -18,9 +18,10 @@ constexpr int64_t kSplitFirstLayerBytes = int64_t(16) << 20;
 // Layers of a signalling launch are waited for in groups of at least this
 // many bytes (all pools), on the flag of the group's last layer, which covers
 // every earlier layer; the group's events are recorded together.  Each stream
-// memory wait and event record costs the GPU's front end about a microsecond,
-// which a burst of small layers would otherwise pay per layer.  Layers of
-// this size or more are waited for one by one.
+// memory wait costs the host about 0.6 us to enqueue, which a burst of small
+// layers would otherwise pay per layer (89 against 30 us of host time for a
+// one-page 78-layer burst).  Layers of this size or more are waited for one by
+// one.
 constexpr int64_t kSignalGroupBytes = int64_t(2) << 20;
 
 // True when the driver provides the stream memory wait the burst relies on.
