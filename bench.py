@@ -1226,7 +1226,7 @@ def run_latency(args, reps=30):
         # the same calls through the C ABI with every argument built beforehand:
         # the library's own host time, without the Python binding's marshalling
         lib = hk.lib()
-        arr, npools, keep = B._pools_arg(pools)
+        arr, npools, _keep = B._pools_arg(pools)  # _keep: pointer arrays arr points into
         co = B._opts_arg(opts, dt, ht)
         sh = stream.cuda_stream
         ev_h = (ctypes.c_void_p * L)(*[B._event_handle(e, sh) for e in evs])

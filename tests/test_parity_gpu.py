@@ -126,15 +126,18 @@ def test_tiny_mha_backup_then_load(where, dtype, path):
             assert np.array_equal(a, b)
 
 
-@pytest.mark.parametrize("pages", [1, 63, 64, 65, 128, 129])
+# The page counts the pages' unit test probes, then the counts whose staged part
+# (a staged backup moves its last eighth of pages zero-copy) is 63/64/65/128/129.
+@pytest.mark.parametrize("pages", [1, 63, 64, 65, 128, 129, 72, 74, 75, 147, 148])
 @pytest.mark.parametrize("path", ["zero_copy", "zero_copy_single_launch", "staged"])
 def test_boundary_page_counts(pages, path):
     """The page counts the pages' unit test probes, through the CUDA path.
 
-    The staging buffers hold exactly 64 pages of all layers, so 63/64/65 and
-    128/129 pages fall just inside, on and just past the staged path's chunk
-    boundaries (backup chunks of 64 pages; load groups of 1 and 2 layers in
-    chunks of 192 and 96 pages).
+    The staging buffers hold exactly 64 pages of all layers. A staged backup
+    copies all but the last eighth of its pages through them (72/74/75 pages:
+    63/64/65 staged, 147/148: 128/129), so those fall just inside, on and just
+    past its chunk boundaries. A 3-layer staged load reads its first layer
+    zero-copy and copies the other two as one group, in chunks of 96 pages.
     """
     s = G.shape(L=3, T=2, head_num=2, head_dim=64, dtype_size=2, P=16, slots=16 * 300, pages=160)
     pool = G.make_pool(s, seed=40 + pages)

@@ -10,8 +10,10 @@ Checked here:
   - on two calls in a row (the second reuses the array the first one left
     behind), the host pool equals, byte for byte, both the CPU oracle's backup
     of the same pairs and what hicache_backup_all_layers writes;
-  - page counts just below, on and just past the 16 MiB half of the array, and
-    a list of three chunks, so that one call refills a half it used before;
+  - page counts whose staged part (all but the last eighth of the pages, which
+    move zero-copy) lies just below, on and just past the 16 MiB half of the
+    array, and a list of three chunks, so that one call refills a half it used
+    before;
   - in a fresh process, once a call with no pairs has done the set-up, later
     calls take no device memory at all.
 
@@ -88,11 +90,13 @@ def _mla_dsa_shapes():
     return [lat, idx]
 
 
-# (shapes, pages per call): 31 / 32 / 33 pages sit just below, on and one past a half;
-# 70 pages are three chunks (32 + 32 + 6), so the third refills the first half within
-# one call; the two-pool case has 481.5 KiB pages, 34 per half, 50 pages over both
-CASES = {"mha31": (_mha_shape, 31), "mha32": (_mha_shape, 32), "mha33": (_mha_shape, 33),
-         "mha70": (_mha_shape, 70), "mla_dsa50": (_mla_dsa_shapes, 50)}
+# (shapes, pages per call).  The staged backup moves the last ceil(pages / 8) pages
+# zero-copy, so 36 / 37 / 38 pages put 31 / 32 / 33 pages through the array: just
+# below, on and one past a half.  75 pages put 65 through it, three chunks (32 + 32
+# + 1), so the third refills the first half within one call.  The two-pool case has
+# 481.5 KiB pages, 34 per half; 50 pages put 43 through it, over both halves.
+CASES = {"mha36": (_mha_shape, 36), "mha37": (_mha_shape, 37), "mha38": (_mha_shape, 38),
+         "mha75": (_mha_shape, 75), "mla_dsa50": (_mla_dsa_shapes, 50)}
 
 
 @pytest.mark.parametrize("case", sorted(CASES))
