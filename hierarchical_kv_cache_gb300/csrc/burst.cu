@@ -128,8 +128,16 @@ hicache_status signaled_burst(const std::vector<PoolInfo>& pools, const SideSpec
     first = 1;
   }
   const int32_t nsig = count - first;
+  // Layers per group: one for layers of kSignalGroupBytes or more, else as
+  // many as make up that size, no more than one launch holds.
+  int32_t segs_per_layer = 0;
+  for (const PoolInfo& pi : pools) segs_per_layer += pi.T;
+  const int64_t per_group = std::min<int64_t>(
+      {int64_t(nsig), kMaxSegLarge / segs_per_layer,
+       std::max<int64_t>(1, (kSignalGroupBytes + layer_bytes - 1) / std::max<int64_t>(1, layer_bytes))});
   uint32_t* words = o.burst_words;
-  BurstWords bw{words, words + nsig, words + 2 * int64_t(nsig), words + 3 * int64_t(nsig)};
+  BurstWords bw{words, words + nsig, words + 2 * int64_t(nsig), words + 3 * int64_t(nsig),
+                int32_t(std::max<int64_t>(1, per_group))};
   cudaError_t e = cudaMemsetAsync(words, 0, size_t(kBurstWordsPerLayer) * nsig * sizeof(uint32_t),
                                   stream);
   if (e == cudaSuccess) e = cudaEventRecord(r->fork, stream);
@@ -146,15 +154,14 @@ hicache_status signaled_burst(const std::vector<PoolInfo>& pools, const SideSpec
     record_from(evs, first, count, stream);
     return st;
   }
-  // one wait per group of layers holding kSignalGroupBytes (one per layer for
-  // layers that large): the flag of the group's last layer covers the group
-  const int32_t per_group = int32_t(std::max<int64_t>(
-      1, std::min<int64_t>(count, (kSignalGroupBytes + layer_bytes - 1) / std::max<int64_t>(1, layer_bytes))));
+  // one wait per group, on the group's own word, then the group's events
+  const int32_t lpg = bw.layers_per_group;
   int32_t i = first;
   while (i < count) {
-    const int32_t last = std::min(count, i + per_group) - 1;
+    const int32_t group = (i - first) / lpg;
+    const int32_t last = std::min(count, first + (group + 1) * lpg) - 1;
     const CUresult cr = wait(reinterpret_cast<CUstream>(r->sig),
-                             reinterpret_cast<CUdeviceptr>(bw.flag + (last - first)), 1u,
+                             reinterpret_cast<CUdeviceptr>(bw.flag + group), 1u,
                              CU_STREAM_WAIT_VALUE_GEQ);
     if (cr != CUDA_SUCCESS) {
       st = fail(HICACHE_ECUDA, "cuStreamWaitValue32 failed with CUresult " + std::to_string(int(cr)));

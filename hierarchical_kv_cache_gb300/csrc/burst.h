@@ -15,13 +15,14 @@ constexpr int kBurstWordsPerLayer = 4;
 // (about 20 us of fixed cost per burst).
 constexpr int64_t kSplitFirstLayerBytes = int64_t(16) << 20;
 
-// Layers of a signalling launch are waited for in groups of at least this
-// many bytes (all pools), on the flag of the group's last layer, which covers
-// every earlier layer; the group's events are recorded together.  Each stream
-// memory wait costs the host about 0.6 us to enqueue, which a burst of small
-// layers would otherwise pay per layer (89 against 30 us of host time for a
-// one-page 78-layer burst).  Layers of this size or more are waited for one by
-// one.
+// Layers of a signalling launch are counted and waited for in groups of at
+// least this many bytes (all pools): the kernel sets one word per group once
+// the group's layers have landed, and the group's events are recorded
+// together after one stream wait.  Each stream memory wait costs the host
+// about 0.6 us to enqueue, which a burst of small layers would otherwise pay
+// per layer (89 against 30 us of host time for a one-page 78-layer burst).
+// Layers of this size or more are groups of their own, so each layer's event
+// comes as soon as it lands.
 constexpr int64_t kSignalGroupBytes = int64_t(2) << 20;
 
 // True when the driver provides the stream memory wait the burst relies on.

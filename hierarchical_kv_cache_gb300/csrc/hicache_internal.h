@@ -74,13 +74,17 @@ struct Segment {
   int32_t pad;
 };
 
-// Per-layer completion signalling of a single-launch burst.  Segments are
-// ordered layer-major, segs_per_layer per layer; layer k of the launch is
-// burst layer layer_base + k.  Words (device memory, zeroed before the launch):
-// done[burst layer] counts finished tasks, flag[burst layer] becomes 1 once
-// every task of that layer and of every earlier layer of the burst has landed
-// (so one flag covers a group of layers); exits[launch first layer] counts
-// CTAs that left the launch and next[launch first layer] hands out its tasks.
+// Completion signalling of a single-launch burst, per group of consecutive
+// layers.  Segments are ordered layer-major, segs_per_layer per layer; layer k
+// of the launch is burst layer layer_base + k, in group (layer_base + k) /
+// layers_per_group.  A launch starts on a group boundary.  Words (device
+// memory, zeroed before the launch): done[group] counts finished tasks,
+// flag[group] becomes 1 once every task of that group's layers has landed;
+// exits[launch first layer] counts CTAs that left the launch and
+// next[launch first layer] hands out its tasks.  Groups are one layer for
+// layers of 2 MiB or more, so a consumer can start on each as it lands, and
+// several small layers otherwise, so the burst pays its stream waits per
+// group rather than per layer.
 struct SignalSpec {
   uint32_t* done = nullptr;
   uint32_t* flag = nullptr;
@@ -88,8 +92,10 @@ struct SignalSpec {
   uint32_t* next = nullptr;
   int64_t tasks_per_layer = 0;
   int32_t segs_per_layer = 0;
-  int32_t layer_base = 0;   // burst-relative index of this launch's first layer
-  int32_t nlayers = 0;      // layers covered by this launch
+  int32_t layer_base = 0;        // burst-relative index of this launch's first layer
+  int32_t nlayers = 0;           // layers covered by this launch
+  int32_t layers_per_group = 1;  // layers counted by one done/flag word
+  int32_t burst_layers = 0;      // signalled layers of the whole burst (all launches)
   int32_t pad = 0;
 };
 
@@ -193,14 +199,16 @@ void fill_geometry(const PoolInfo& pi, int64_t npairs, int vec, int64_t paged_pa
                    int64_t paged_tokens, int32_t rows_per_page, PoolGeom* g);
 // Moves pairs [pair_begin, pair_begin + npairs) for layers [layer_begin, layer_end)
 // of every pool and tensor between the device buffers and `side`.  With
-// `signal` (words of a single-launch burst: done, flag, exits, next, each
-// indexed by l - layer_begin), launches are cut at layer boundaries and every layer's flag
-// word is set once all of its rows have landed.
+// `signal` (words of a single-launch burst: done and flag indexed by group
+// (l - layer_begin) / layers_per_group, exits and next by l - layer_begin),
+// launches are cut at group boundaries and every group's flag word is set once
+// all of its rows have landed.
 struct BurstWords {
   uint32_t* done = nullptr;
   uint32_t* flag = nullptr;
   uint32_t* exits = nullptr;
   uint32_t* next = nullptr;
+  int32_t layers_per_group = 1;  // launches are cut only at multiples of this many layers
 };
 hicache_status launch_rows(const std::vector<PoolInfo>& pools, const SideSpec& side,
                            const void* dev_idx, const void* paged_idx, int32_t index_bits,

@@ -33,42 +33,23 @@ __device__ __forceinline__ uint32_t ld_stream(const uint32_t* p) { return __ldcs
 __device__ __forceinline__ void st_stream(uint4* p, const uint4& v) { __stcs(p, v); }
 __device__ __forceinline__ void st_stream(uint32_t* p, const uint32_t& v) { __stcs(p, v); }
 
-// Burst-relative layer l has just completed.  Publishes its flag and the flags
-// of the complete layers after it, as long as every earlier layer is
-// published, so that flag[l] set means layers 0..l of the burst's signalled
-// range have all landed: a stream wait on one flag covers a whole group of
-// layers.  A completion that finds the layer before it unpublished stops
-// there; the warp that publishes that layer then finds this one complete and
-// carries on.  Both sides write (their done count, or a flag), fence and then
-// read the other side's word, so at least one of them sees the other's write
-// (publishing twice is harmless).  Called by one lane.
+// Adds `count` finished tasks to burst group `group`; the warp that completes
+// the group publishes its flag.  A group is layers_per_group consecutive layers
+// (the last group of the burst may hold fewer).  Called by all 32 lanes of a
+// warp.
 template <int MAXSEG>
-__device__ __forceinline__ void publish_from(const CopyParams<MAXSEG>& p, int l) {
-  const int end = p.sig.layer_base + p.sig.nlayers;
-  for (;;) {
-    __threadfence();
-    if (l > 0 && *reinterpret_cast<volatile const uint32_t*>(&p.sig.flag[l - 1]) == 0) return;
-    atomicExch(&p.sig.flag[l], 1u);
-    __threadfence();
-    if (++l >= end) return;
-    if (int64_t(*reinterpret_cast<volatile const uint32_t*>(&p.sig.done[l])) !=
-        p.sig.tasks_per_layer)
-      return;
-  }
-}
-
-// Adds `count` finished tasks to burst layer `layer`; the warp that completes
-// the layer publishes its flag (and those after it, see publish_from).  Called
-// by all 32 lanes of a warp.
-template <int MAXSEG>
-__device__ __forceinline__ void flush_layer(const CopyParams<MAXSEG>& p, int layer,
+__device__ __forceinline__ void flush_group(const CopyParams<MAXSEG>& p, int group,
                                             uint32_t count, int lane) {
-  __threadfence();  // this lane's stores of the layer are visible device-wide
+  __threadfence();  // this lane's stores of the group are visible device-wide
   __syncwarp();
   if (lane == 0) {
-    const int l = p.sig.layer_base + layer;
-    const uint32_t before = atomicAdd(&p.sig.done[l], count);
-    if (int64_t(before) + count == p.sig.tasks_per_layer) publish_from(p, l);
+    const int lpg = p.sig.layers_per_group;
+    const int layers = min(lpg, p.sig.burst_layers - group * lpg);
+    const uint32_t before = atomicAdd(&p.sig.done[group], count);
+    if (int64_t(before) + count == p.sig.tasks_per_layer * layers) {
+      __threadfence();
+      atomicExch(&p.sig.flag[group], 1u);
+    }
   }
 }
 
@@ -269,32 +250,36 @@ __global__ void __launch_bounds__(kThreadsPerCta)
     // on the tasks still in flight when its last one was taken.  The next task
     // is claimed before the current one is copied, hiding the atomic's latency.
     uint32_t* next = p.sig.next + p.sig.layer_base;
-    int cur_layer = -1;    // launch-relative layer of the tasks counted in `pending`
-    uint32_t pending = 0;  // finished tasks of cur_layer not yet added to its counter
+    const int lpg = p.sig.layers_per_group;
+    int cur_group = -1;    // burst group of the tasks counted in `pending`
+    uint32_t pending = 0;  // finished tasks of cur_group not yet added to its counter
     uint32_t claim = lane == 0 ? atomicAdd(next, 1u) : 0u;
     int64_t task = __shfl_sync(0xffffffffu, claim, 0);
     while (task < ntasks) {
       claim = lane == 0 ? atomicAdd(next, 1u) : 0u;
       const int layer = copy_task<IdxT, MAXSEG, false, DEEP4>(p, task, lane, offs) / p.sig.segs_per_layer;
-      if (layer != cur_layer) {
-        if (pending != 0) flush_layer(p, cur_layer, pending, lane);
-        cur_layer = layer;
+      const int group = (p.sig.layer_base + layer) / lpg;
+      if (group != cur_group) {
+        if (pending != 0) flush_group(p, cur_group, pending, lane);
+        cur_group = group;
         pending = 0;
       }
       ++pending;
       task = __shfl_sync(0xffffffffu, claim, 0);
     }
-    if (pending != 0) flush_layer(p, cur_layer, pending, lane);
-    // The last CTA to leave sets every flag of this launch's layers.  All tasks
-    // have been counted by then, so this only guarantees that no waiter can
-    // outlive the launch.
+    if (pending != 0) flush_group(p, cur_group, pending, lane);
+    // The last CTA to leave sets every flag of this launch's groups (a launch
+    // covers whole groups).  All tasks have been counted by then, so this only
+    // guarantees that no waiter can outlive the launch.
     __syncthreads();
     if (threadIdx.x == 0) {
       __threadfence();
       const uint32_t gone = atomicAdd(&p.sig.exits[p.sig.layer_base], 1u);
       if (gone == gridDim.x - 1) {
         __threadfence();
-        for (int k = 0; k < p.sig.nlayers; ++k) atomicExch(&p.sig.flag[p.sig.layer_base + k], 1u);
+        const int g0 = p.sig.layer_base / lpg;
+        const int g1 = (p.sig.layer_base + p.sig.nlayers - 1) / lpg;
+        for (int g = g0; g <= g1; ++g) atomicExch(&p.sig.flag[g], 1u);
       }
     }
   }

@@ -257,11 +257,14 @@ hicache_status launch_rows(const std::vector<PoolInfo>& pools, const SideSpec& s
       }
       tasks_per_layer += int64_t(pi.T) * g.tasks_per_seg;
     }
-    // A signalling launch covers whole layers only and counts its tasks in
-    // 32-bit words; one layer must fit in one launch.
-    if (signal && tasks_per_layer > kMaxSignalTasks)
-      return fail(HICACHE_EINVAL, "single-launch burst: more than 2^30 tasks in one layer");
+    // A signalling launch covers whole groups of layers only and counts a
+    // group's tasks in a 32-bit word; one group must fit in one launch.
+    const int32_t lpg = signal ? std::max<int32_t>(1, signal->layers_per_group) : 1;
+    if (signal && tasks_per_layer * lpg > kMaxSignalTasks)
+      return fail(HICACHE_EINVAL, "single-launch burst: more than 2^30 tasks in one layer group");
     const int cap = signal ? (maxseg / segs_per_layer) * segs_per_layer : maxseg;
+    if (signal && int64_t(lpg) * segs_per_layer > cap)
+      return fail(HICACHE_EINVAL, "single-launch burst: a layer group is larger than one launch");
     int nseg = 0;
     int64_t tasks = 0;
     int32_t first_layer = layer_begin;
@@ -278,6 +281,8 @@ hicache_status launch_rows(const std::vector<PoolInfo>& pools, const SideSpec& s
         prm.sig.segs_per_layer = segs_per_layer;
         prm.sig.layer_base = first_layer - layer_begin;
         prm.sig.nlayers = next_layer - first_layer;
+        prm.sig.layers_per_group = lpg;
+        prm.sig.burst_layers = layer_end - layer_begin;
         st = launch_segments<std::remove_reference_t<decltype(prm)>::kMaxSeg, true>(
             prm, index_bits, tasks, cfg, stream);
       } else {
@@ -290,10 +295,15 @@ hicache_status launch_rows(const std::vector<PoolInfo>& pools, const SideSpec& s
       return st;
     };
     for (int32_t l = layer_begin; l < layer_end; ++l) {
-      if (nseg + segs_per_layer > cap ||
-          (signal && nseg > 0 && tasks + tasks_per_layer > kMaxSignalTasks)) {
-        const hicache_status st = flush(l);
-        if (st != HICACHE_OK) return st;
+      // a launch is cut only where a group starts, when the whole group
+      // would not fit
+      if ((l - layer_begin) % lpg == 0) {
+        const int64_t gl = std::min<int32_t>(lpg, layer_end - l);
+        if (nseg + gl * segs_per_layer > cap ||
+            (signal && nseg > 0 && tasks + gl * tasks_per_layer > kMaxSignalTasks)) {
+          const hicache_status st = flush(l);
+          if (st != HICACHE_OK) return st;
+        }
       }
       for (size_t p = 0; p < pools.size(); ++p) {
         const PoolInfo& pi = pools[p];

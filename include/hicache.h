@@ -218,12 +218,12 @@ hicache_status hicache_load_layer(const hicache_pool* pools, int32_t num_pools, 
  * a layer holds 16 MiB or more: the first layer alone (its event recorded on
  * `stream`), then one launch covering all other layers; a smaller burst is
  * that one launch alone.  Its tasks are handed out in layer order: the kernel
- * sets one word per layer once that layer and every earlier one have landed,
- * a library stream forked from `stream` waits on the words with stream memory
- * waits and records the layers' events, and `stream` joins that stream before
- * the call returns.  Layers of 2 MiB or more (all pools) get a wait each;
- * smaller layers are waited for in groups of about 2 MiB, whose events are
- * recorded together once the group's last layer has landed.  The words must not be shared by bursts that overlap on the
+ * sets one word per group of layers once the group has landed, a library
+ * stream forked from `stream` waits on each word with a stream memory wait and
+ * records the group's layer events, and `stream` joins that stream before the
+ * call returns.  A layer of 2 MiB or more (all pools) is a group of its own;
+ * smaller layers form groups of about 2 MiB, whose events are recorded together
+ * once the whole group has landed.  The words must not be shared by bursts that overlap on the
  * GPU.  The staged path ignores burst_words.
  * The staged path reads the first layers of a burst of two or more layers
  * zero-copy (the SMs read the host pool; one layer in eight, at least one,
