@@ -5,10 +5,11 @@
  * with cudaMalloc, the page-first host pool with cudaHostAlloc), backs up a
  * list of whole pages with hicache_backup_all_layers, loads them back into
  * other device pages with a single-launch hicache_load_burst, repeats both on
- * the staged path with cudaMalloc'd staging buffers, and checks every byte of
- * both pools against the CPU oracle (test infrastructure, linked only by
- * tests).  Exit status 0 means bit-exact; it prints the first mismatch
- * otherwise.
+ * the staged path with cudaMalloc'd staging buffers, backs up once more with
+ * the allocation-free entry point, and checks every byte of both pools against
+ * the CPU oracle (test infrastructure, linked only by tests).  It also asks
+ * hicache_auto_path for the path.  Exit status 0 means bit-exact; it prints the
+ * first mismatch otherwise.
  */
 #include <stdint.h>
 #include <stdio.h>
@@ -183,9 +184,10 @@ int main(void) {
   for (int l = 0; l < L; ++l) CHECK_CUDA(cudaEventSynchronize(ev[l]));
 
   /* the staged path: backup to other host pages, then a burst into other
-     device pages.  The staging holds 7 host pages of all layers (backup in
-     chunks of 7 + 3 pages), 21 pages of one layer and 10 of two (load groups
-     of 1 and 2 layers, one chunk each). */
+     device pages.  The staging holds 7 host pages of all layers: the backup
+     copies 8 of its 10 pages through it (chunks of 7 + 1) and the last 2
+     zero-copy.  The load reads layer 0 zero-copy and copies layers 1-2 as one
+     group (10 pages of two layers fit in one chunk). */
   int64_t hpages3[NPAGES], dpages3[NPAGES];
   sample(10, HPAGES, NPAGES, hpages, NPAGES, hpages3);
   sample(11, SLOTS / P, NPAGES, dpages, NPAGES, dpages3);
@@ -229,6 +231,43 @@ int main(void) {
         }
     }
   }
+
+  /* the allocation-free backup, as a C caller with no device allocator of its
+     own would use it: one call with no pairs first (the set-up that takes the
+     library's static staging array), then the pairs, to yet other host pages */
+  int64_t hpages4[NPAGES], used[2 * NPAGES];
+  for (int64_t k = 0; k < NPAGES; ++k) {
+    used[k] = hpages[k];
+    used[NPAGES + k] = hpages3[k];
+  }
+  sample(12, HPAGES, NPAGES, used, 2 * NPAGES, hpages4);
+  for (int64_t k = 0; k < NPAGES; ++k)
+    for (int64_t t = 0; t < P; ++t) h_idx[k * P + t] = hpages4[k] * P + t;
+  CHECK_HK(hicache_backup_all_layers_static_staging(&pool, 1, NULL, NULL, 64, 0, NULL, stream));
+  CHECK_HK(hicache_backup_all_layers_static_staging(&pool, 1, d_idx, h_idx, 64, n, NULL, stream));
+  CHECK_CUDA(cudaStreamSynchronize(stream));
+  for (int t = 0; t < T; ++t) {
+    const uint8_t* layers[L];
+    for (int l = 0; l < L; ++l) layers[l] = dev_img[t * L + l];
+    if (oracle_backup_all_layers(L, P, R, SLOTS, HPAGES, layers, host_img[t], d_idx, h_idx, n) != 0)
+      return 4;
+    for (size_t b = 0; b < host_bytes; ++b)
+      if (host[t][b] != host_img[t][b]) {
+        fprintf(stderr, "static-staging backup: tensor %d byte %zu differs\n", t, b);
+        return 1;
+      }
+  }
+
+  /* AUTO's rule from C: with a small CTA budget and staging the rule still
+     says zero-copy here, because these host pages (12 KiB) are far below the
+     1 MiB a staged DMA needs; without a budget it is zero-copy too */
+  int32_t path = -1;
+  sopts.path = HICACHE_PATH_AUTO;
+  sopts.max_ctas = 8;
+  CHECK_HK(hicache_auto_path(&pool, 1, d_idx, h_idx, 64, n, &sopts, HICACHE_OP_BACKUP, 0, &path));
+  if (path != HICACHE_PATH_ZERO_COPY) return 6;
+  CHECK_HK(hicache_auto_path(&pool, 1, d_idx, h_idx, 64, n, NULL, HICACHE_OP_LOAD, L, &path));
+  if (path != HICACHE_PATH_ZERO_COPY) return 6;
 
   printf("c abi round trip ok: %d layers, %d tensors, %d pages, launches %lld\n", L, T, NPAGES,
          (long long)hicache_kernel_launches());
