@@ -36,8 +36,8 @@ hicache_status cuda_fail(cudaError_t e, const std::string& what) {
 struct StagedRes {
   bool init = false;
   cudaStream_t copy = nullptr;
-  cudaStream_t side = nullptr;  // zero-copy share of a staged backup
-  cudaEvent_t fork = nullptr, join = nullptr, side_done = nullptr;
+  cudaStream_t side = nullptr;  // zero-copy share of a staged call
+  cudaEvent_t fork = nullptr, join = nullptr, side_done = nullptr, group_start = nullptr;
   cudaEvent_t ready[2] = {nullptr, nullptr};
   cudaEvent_t freed[2] = {nullptr, nullptr};
 };
@@ -51,8 +51,8 @@ hicache_status get_res(StagedRes** out) {
   if (!r.init) {
     HK_CUDA(cudaStreamCreateWithFlags(&r.copy, cudaStreamNonBlocking), "cudaStreamCreate(copy)");
     HK_CUDA(cudaStreamCreateWithFlags(&r.side, cudaStreamNonBlocking), "cudaStreamCreate(side)");
-    cudaEvent_t* evs[7] = {&r.fork,     &r.join,     &r.side_done, &r.ready[0],
-                           &r.ready[1], &r.freed[0], &r.freed[1]};
+    cudaEvent_t* evs[8] = {&r.fork,     &r.join,     &r.side_done, &r.ready[0],
+                           &r.ready[1], &r.freed[0], &r.freed[1], &r.group_start};
     for (cudaEvent_t* e : evs) HK_CUDA(cudaEventCreateWithFlags(e, cudaEventDisableTiming), "cudaEventCreate");
     r.init = true;
   }
@@ -171,8 +171,8 @@ bool device_pages_consecutive(const void* dev_idx, int32_t bits, int64_t n, int3
 constexpr int64_t kDirectPageBytes = int64_t(1) << 20;
 
 // A staged call moves this fraction of its work (1 / kZeroCopyShare) zero-copy
-// beside the copy engine: the last pages of a backup, the first layers of a
-// load.  The copy engine leaves the link idle for its fixed time per copy
+// beside the copy engine: the last pages of a backup; the first layers of a
+// load, and the last pages of each of its layer groups.  The copy engine leaves the link idle for its fixed time per copy
 // (2.4-3.3 us on GB300) and moves a load's first small layer groups at a
 // fraction of the link; SM-issued traffic beside it fills those gaps.
 constexpr int64_t kZeroCopyShare = 8;
@@ -355,14 +355,17 @@ hicache_status staged_load(const std::vector<PoolInfo>& all_pools, const hicache
   const int32_t count = layer_end - layer_begin;
   int32_t recorded = 0;  // layer events recorded so far, in order
   cudaStream_t forked = nullptr;  // the copy stream once it has forked from `stream`
+  bool side_used = false;         // the side stream holds zero-copy page shares
   StagedRes* r = nullptr;
   auto finish = [&](hicache_status s) {
     // A failed load joins the copy stream back into `stream` (copies into the
-    // staging buffers may still be in flight) and then completes every
-    // remaining layer event.
+    // staging buffers may still be in flight), and the side stream, and then
+    // completes every remaining layer event.
     if (forked) {
       cudaError_t e = cudaEventRecord(r->join, forked);
       if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, r->join, 0);
+      if (e == cudaSuccess && side_used) e = cudaEventRecord(r->side_done, r->side);
+      if (e == cudaSuccess && side_used) e = cudaStreamWaitEvent(stream, r->side_done, 0);
       if (e != cudaSuccess && s == HICACHE_OK) s = cuda_fail(e, "staged load join");
     }
     for (int32_t i = recorded; i < count; ++i)
@@ -386,6 +389,10 @@ hicache_status staged_load(const std::vector<PoolInfo>& all_pools, const hicache
   const LaunchCfg zero_copy{o.max_ctas, o.device_error, /*paged_in_hbm=*/false};
   const int64_t groups = int64_t(hp.size());
   if (groups == 0) return finish(HICACHE_OK);  // nothing to move; the events still fire
+  // The last pages of every layer group (kZeroCopyShare) are read zero-copy
+  // on the side stream while the copy engine moves the group's other pages.
+  const int64_t zc_pages = groups >= kZeroCopyShare ? (groups + kZeroCopyShare - 1) / kZeroCopyShare : 0;
+  const int64_t dma_groups = groups - zc_pages;
   const bool dev_consecutive = device_pages_consecutive(idx.dev_cpu, idx.bits, idx.n, P);
   int64_t max_block = 1;
   for (const PoolInfo& pi : pools) max_block = std::max(max_block, int64_t(pi.P) * pi.token_bytes);
@@ -451,16 +458,26 @@ hicache_status staged_load(const std::vector<PoolInfo>& all_pools, const hicache
     if (remaining > g && remaining - g < g) g = remaining <= g_cap ? remaining : (remaining + 1) / 2;
     // the largest such group whose chunks hold kMinChunkPages pages, or every
     // page; one layer per group when not even that fits
-    while (g > 1 && layout_for(pools, o, g).cap_pages < std::min(groups, kMinChunkPages)) --g;
+    while (g > 1 && layout_for(pools, o, g).cap_pages < std::min(dma_groups, kMinChunkPages)) --g;
     g_want = std::min(g_cap, kGroupGrowth * g_want);
     const StagingLayout lay = layout_for(pools, o, g);
-    for (int64_t g0 = 0; g0 < groups; g0 += lay.cap_pages, ++step) {
+    for (int64_t g0 = 0; g0 < dma_groups; g0 += lay.cap_pages, ++step) {
       const int b = int(step & 1);
-      const int64_t g1 = std::min(groups, g0 + lay.cap_pages);
-      const bool last_chunk = g1 == groups;
+      const int64_t g1 = std::min(dma_groups, g0 + lay.cap_pages);
+      const bool last_chunk = g1 == dma_groups;
       const SideSpec side = staging_side(pools, lay, static_cast<char*>(o.staging[b]), g, l);
       // the scatter of step-2 must have read buffer b before the DMA refills it
       if (step >= 2) HK_TRY(cudaStreamWaitEvent(copy, r->freed[b], 0), "cudaStreamWaitEvent(freed)");
+      if (g0 == 0 && zc_pages > 0) {
+        // the group's zero-copy pages start with its first copies
+        HK_TRY(cudaEventRecord(r->group_start, copy), "cudaEventRecord(group start)");
+        HK_TRY(cudaStreamWaitEvent(r->side, r->group_start, 0), "cudaStreamWaitEvent(group start)");
+        side_used = true;
+        st = launch_rows(all_pools, host_side(all_pools), idx.dev_gpu, idx.host_gpu, idx.bits,
+                         dma_groups * P, zc_pages * P, kPagedToDev, l, l + g, zero_copy, r->side);
+        if (st != HICACHE_OK) return finish(st);
+        HK_TRY(cudaEventRecord(r->side_done, r->side), "cudaEventRecord(side done)");
+      }
       for (size_t p = 0; p < pools.size(); ++p) {
         const PoolInfo& pi = pools[p];
         const int64_t R = pi.token_bytes;
@@ -497,7 +514,10 @@ hicache_status staged_load(const std::vector<PoolInfo>& all_pools, const hicache
         if (st == HICACHE_OK) st = move_direct(g0, g1, l, l + g);
         if (st != HICACHE_OK) return finish(st);
       } else {
-        // the group's last chunk: scatter layer by layer, each followed by its event
+        // the group's last chunk: scatter layer by layer, each followed by its
+        // event, which also waits for the group's zero-copy pages
+        if (zc_pages > 0)
+          HK_TRY(cudaStreamWaitEvent(stream, r->side_done, 0), "cudaStreamWaitEvent(side done)");
         for (int32_t k = l; k < l + g; ++k) {
           st = move_staging(pools, side, idx, dev_consecutive, g0, g1, kPagedToDev, k, k + 1, cfg,
                             stream);

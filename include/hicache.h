@@ -232,7 +232,9 @@ hicache_status hicache_load_layer(const hicache_pool* pools, int32_t num_pools, 
  * about 4 MiB per copy, in chunks of pages that fit a staging buffer), and
  * scatters and records the events of a group's layers one by one.  Its later
  * layer events therefore arrive in groups, each no earlier than its own
- * layer's data.  A pool whose host page is under 1 MiB beside a larger pool
+ * layer's data.  The last eighth of the pages of each group is read zero-copy
+ * on a library stream while the copy engine moves the group's other pages;
+ * the group's events also wait for it.  A pool whose host page is under 1 MiB beside a larger pool
  * moves zero-copy throughout.  The staged backup likewise moves the last
  * eighth of its pages, and such small pools, zero-copy on a library stream
  * beside its DMAs.
