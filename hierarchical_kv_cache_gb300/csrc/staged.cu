@@ -393,6 +393,7 @@ hicache_status staged_load(const std::vector<PoolInfo>& all_pools, const hicache
   // on the side stream while the copy engine moves the group's other pages.
   const int64_t zc_pages = groups >= kZeroCopyShare ? (groups + kZeroCopyShare - 1) / kZeroCopyShare : 0;
   const int64_t dma_groups = groups - zc_pages;
+  const bool group_side = zc_pages > 0 || !direct.empty();  // a group has side-stream work
   const bool dev_consecutive = device_pages_consecutive(idx.dev_cpu, idx.bits, idx.n, P);
   int64_t max_block = 1;
   for (const PoolInfo& pi : pools) max_block = std::max(max_block, int64_t(pi.P) * pi.token_bytes);
@@ -440,12 +441,6 @@ hicache_status staged_load(const std::vector<PoolInfo>& all_pools, const hicache
     if (st != HICACHE_OK) return finish(st);
   }
   const int32_t first = layer_begin + zc_layers;
-  // The small pools' share of a scatter step: zero-copy from the host pool.
-  auto move_direct = [&](int64_t g0, int64_t g1, int32_t l0, int32_t l1) {
-    if (direct.empty()) return HICACHE_OK;
-    return launch_rows(direct, direct_side, idx.dev_gpu, idx.host_gpu, idx.bits, g0 * P,
-                       (g1 - g0) * P, kPagedToDev, l0, l1, zero_copy, stream);
-  };
   int64_t step = 0;
   // the groups start small whatever the zero-copy share, so that the layer
   // events keep arriving in steps (a consumer starts on them early)
@@ -468,14 +463,24 @@ hicache_status staged_load(const std::vector<PoolInfo>& all_pools, const hicache
       const SideSpec side = staging_side(pools, lay, static_cast<char*>(o.staging[b]), g, l);
       // the scatter of step-2 must have read buffer b before the DMA refills it
       if (step >= 2) HK_TRY(cudaStreamWaitEvent(copy, r->freed[b], 0), "cudaStreamWaitEvent(freed)");
-      if (g0 == 0 && zc_pages > 0) {
-        // the group's zero-copy pages start with its first copies
+      if (g0 == 0 && group_side) {
+        // The group's zero-copy work starts with its first copies, on the side
+        // stream: the staged pools' last pages, and every page of the small
+        // pools.  One launch each per group keeps the launch count low, which
+        // matters when a concurrent kernel holds the SMs.
         HK_TRY(cudaEventRecord(r->group_start, copy), "cudaEventRecord(group start)");
         HK_TRY(cudaStreamWaitEvent(r->side, r->group_start, 0), "cudaStreamWaitEvent(group start)");
         side_used = true;
-        st = launch_rows(all_pools, host_side(all_pools), idx.dev_gpu, idx.host_gpu, idx.bits,
-                         dma_groups * P, zc_pages * P, kPagedToDev, l, l + g, zero_copy, r->side);
-        if (st != HICACHE_OK) return finish(st);
+        if (zc_pages > 0) {
+          st = launch_rows(pools, host_side(pools), idx.dev_gpu, idx.host_gpu, idx.bits,
+                           dma_groups * P, zc_pages * P, kPagedToDev, l, l + g, zero_copy, r->side);
+          if (st != HICACHE_OK) return finish(st);
+        }
+        if (!direct.empty()) {
+          st = launch_rows(direct, direct_side, idx.dev_gpu, idx.host_gpu, idx.bits, 0, idx.n,
+                           kPagedToDev, l, l + g, zero_copy, r->side);
+          if (st != HICACHE_OK) return finish(st);
+        }
         HK_TRY(cudaEventRecord(r->side_done, r->side), "cudaEventRecord(side done)");
       }
       for (size_t p = 0; p < pools.size(); ++p) {
@@ -508,21 +513,15 @@ hicache_status staged_load(const std::vector<PoolInfo>& all_pools, const hicache
       }
       HK_TRY(cudaEventRecord(r->ready[b], copy), "cudaEventRecord(ready)");
       HK_TRY(cudaStreamWaitEvent(stream, r->ready[b], 0), "cudaStreamWaitEvent(ready)");
-      if (!last_chunk) {
-        st = move_staging(pools, side, idx, dev_consecutive, g0, g1, kPagedToDev, l, l + g, cfg,
-                          stream);
-        if (st == HICACHE_OK) st = move_direct(g0, g1, l, l + g);
-        if (st != HICACHE_OK) return finish(st);
-      } else {
-        // the group's last chunk: scatter layer by layer, each followed by its
-        // event, which also waits for the group's zero-copy pages
-        if (zc_pages > 0)
+      // one scatter launch per chunk, all of the group's layers
+      st = move_staging(pools, side, idx, dev_consecutive, g0, g1, kPagedToDev, l, l + g, cfg,
+                        stream);
+      if (st != HICACHE_OK) return finish(st);
+      if (last_chunk) {
+        // the group has landed once its zero-copy work has too: its events
+        if (group_side)
           HK_TRY(cudaStreamWaitEvent(stream, r->side_done, 0), "cudaStreamWaitEvent(side done)");
         for (int32_t k = l; k < l + g; ++k) {
-          st = move_staging(pools, side, idx, dev_consecutive, g0, g1, kPagedToDev, k, k + 1, cfg,
-                            stream);
-          if (st == HICACHE_OK) st = move_direct(g0, g1, k, k + 1);
-          if (st != HICACHE_OK) return finish(st);
           if (layer_done && layer_done[k - layer_begin])
             HK_TRY(cudaEventRecord(layer_done[k - layer_begin], stream), "cudaEventRecord(layer_done)");
           ++recorded;

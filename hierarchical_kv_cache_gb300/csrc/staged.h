@@ -14,9 +14,11 @@ namespace hk {
 hicache_status staged_backup(const std::vector<PoolInfo>& pools, const hicache_opts& o,
                              const IndexSet& idx, cudaStream_t stream);
 
-// Per-layer load-back through HBM staging: per layer, 2-D DMAs of the layer's
-// block of every host page run into staging, then a scatter kernel into the
-// device slots; layer_done[l - layer_begin] is recorded after layer l.
+// Load-back through HBM staging: after the first layers (read zero-copy), per
+// group of consecutive layers, 2-D DMAs of the group's blocks of every host
+// page run into staging and one scatter kernel per staging chunk into the
+// device slots; layer_done[l - layer_begin] is recorded once layer l's group
+// has landed.
 hicache_status staged_load(const std::vector<PoolInfo>& pools, const hicache_opts& o,
                            const IndexSet& idx, int32_t layer_begin, int32_t layer_end,
                            cudaStream_t stream, cudaEvent_t* layer_done);

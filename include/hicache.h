@@ -229,13 +229,14 @@ hicache_status hicache_load_layer(const hicache_pool* pools, int32_t num_pools, 
  * zero-copy (the SMs read the host pool; one layer in eight, at least one,
  * each with its own launch and event), then copies groups of consecutive
  * layers of each host page per DMA, each group four times the previous (up to
- * about 4 MiB per copy, in chunks of pages that fit a staging buffer), and
- * scatters and records the events of a group's layers one by one.  Its later
- * layer events therefore arrive in groups, each no earlier than its own
- * layer's data.  The last eighth of the pages of each group is read zero-copy
- * on a library stream while the copy engine moves the group's other pages;
- * the group's events also wait for it.  A pool whose host page is under 1 MiB beside a larger pool
- * moves zero-copy throughout.  The staged backup likewise moves the last
+ * about 4 MiB per copy, in chunks of pages that fit a staging buffer),
+ * scatters each chunk in one launch, and records a group's events once its
+ * last chunk has landed.  Its later layer events therefore arrive in groups,
+ * each no earlier than its own layer's data.  The last eighth of the pages
+ * of each group is read zero-copy on a library stream while the copy engine
+ * moves the group's other pages, and so is a pool whose host page is under
+ * 1 MiB beside a larger pool (one launch each per group); the group's events
+ * also wait for that stream.  The staged backup likewise moves the last
  * eighth of its pages, and such small pools, zero-copy on a library stream
  * beside its DMAs.
  */
