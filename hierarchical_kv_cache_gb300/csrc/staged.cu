@@ -16,6 +16,7 @@
 #include <string>
 #include <vector>
 
+#include "burst.h"
 #include "staged.h"
 
 namespace hk {
@@ -436,9 +437,19 @@ hicache_status staged_load(const std::vector<PoolInfo>& all_pools, const hicache
   HK_TRY(cudaEventRecord(r->fork, stream), "cudaEventRecord(fork)");
   HK_TRY(cudaStreamWaitEvent(copy, r->fork, 0), "cudaStreamWaitEvent(fork)");
   forked = copy;
-  for (int32_t k = layer_begin + 1; k < layer_begin + zc_layers; ++k) {
-    st = load_direct_layer(k);
+  if (zc_layers >= 3 && o.burst_words && signaled_burst_available()) {
+    // the other zero-copy layers as one signalling launch (fewer launches to
+    // wait for SMs when a concurrent kernel holds them); it records their
+    // events on every return path
+    st = signaled_burst(all_pools, host_side(all_pools), idx, o, layer_begin + 1,
+                        layer_begin + zc_layers, stream, layer_done ? layer_done + 1 : nullptr);
+    recorded += zc_layers - 1;
     if (st != HICACHE_OK) return finish(st);
+  } else {
+    for (int32_t k = layer_begin + 1; k < layer_begin + zc_layers; ++k) {
+      st = load_direct_layer(k);
+      if (st != HICACHE_OK) return finish(st);
+    }
   }
   const int32_t first = layer_begin + zc_layers;
   int64_t step = 0;

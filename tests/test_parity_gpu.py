@@ -172,6 +172,44 @@ def test_boundary_page_counts(pages, path):
     G.assert_device_equal(pool, dev1, f"{pages} pages burst")
 
 
+@pytest.mark.parametrize("case", ["latent_and_indexer_78_layers", "mha_24_layers"])
+def test_staged_burst_with_burst_words(case):
+    """A staged burst given burst_words, bit for bit against the oracle.
+
+    Its first layers (one in eight) are read zero-copy: layer 0 with a launch of
+    its own, the others as one signalling launch whose events a library stream
+    records.  The groups after them go through staging.  The events are checked
+    to be recorded by the call, behind a sleep on the caller's stream.
+    """
+    if case == "latent_and_indexer_78_layers":
+        lat = G.shape("lat", L=78, T=1, head_num=1, head_dim=576, dtype_size=2, P=64,
+                      slots=64 * 48, pages=48)
+        idx = G.shape("idx", L=78, T=1, head_num=1, head_dim=132, dtype_size=1, P=64,
+                      slots=64 * 48, pages=48, page_granular=True, value_kind="uint8_uniform")
+        shapes, pages = [lat, idx], 20
+    else:
+        shapes, pages = [G.shape("mha", L=24, T=2, head_num=2, head_dim=64, dtype_size=2, P=16,
+                                 slots=16 * 96, pages=64)], 30
+    pools = [G.make_pool(s, 60 + k) for k, s in enumerate(shapes)]
+    s0 = shapes[0]
+    L, P = s0.num_layers, s0.page_size
+    d, h, _, _ = W.page_pairs(61, pages, s0.device_slots // P, s0.host_pages, P)
+    dt, ht = G.index_tensors(d, h, "host")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    opts = _opts(hk.HICACHE_PATH_STAGED, "host", staging=_staging(16 << 20),
+                 burst_words=_burst_words(L), device_error=err)
+    dev0 = [G.device_images(p) for p in pools]
+    host0 = [G.host_images(p) for p in pools]
+    events = [torch.cuda.Event() for _ in range(L)]
+    _arm(events)
+    hk.hicache_load_burst(pools, 0, L, ht, dt, opts=opts, layer_done=events)
+    _assert_recorded_behind_sleep(events)
+    assert int(err.item()) == 0
+    for p, dv, hs in zip(pools, dev0, host0):
+        G.oracle_load(p, dv, hs, range(L), h, d)
+        G.assert_device_equal(p, dv, f"{case}: staged burst with burst_words")
+
+
 # ------------------------------------------------------ ragged shapes and tails
 
 CASES = [
