@@ -22,6 +22,16 @@ constexpr int kThreadsPerCta = kWarpsPerCta * 32;
 constexpr int kUnroll = 4;          // chunks in flight per lane per iteration
 constexpr int kMaxRowsPerTask = 128; // rows of one warp task (shared-memory offset table)
 constexpr int64_t kTaskBytes = 2048; // target payload of one warp task
+// Deep tasks, for launches with few CTAs against the host pool: twice the
+// payload per task and twice the chunks in flight per lane, so that each warp
+// keeps twice the bytes outstanding on the host link.  Measured on GB300 with
+// 16 CTAs: a Llama-3-8B burst 157 against 93 GB/s, a 78-layer backup 177
+// against 117.  With one CTA per SM they cost a concurrent GEMM more (their
+// registers crowd it out: 39 against 27 % during a burst) and move no more, so
+// launches of more than kDeepMaxCtas CTAs keep the shallow tasks.
+constexpr int kUnrollDeep = 8;
+constexpr int64_t kTaskBytesDeep = 4096;
+constexpr int kDeepMaxCtas = 76;
 constexpr int kMaxSegSmall = 8;     // per-layer launches: pools x tensors
 constexpr int kMaxSegLarge = 512;   // all-layer launches: pools x tensors x layers
 // A signalling launch hands out its tasks from a 32-bit counter that every warp
@@ -154,19 +164,22 @@ hicache_status plan_runs(const void* dev_idx, const void* host_idx, int32_t inde
                          int64_t* full_pages);
 
 // Launch-side helpers (zero_copy.cu).
-// Default CTAs per SM of a copy launch (256 threads each).  Measured on GB300:
+// Default CTAs of a copy launch (256 threads each).  Measured on GB300:
 // one CTA per SM reaches the host-link peak in either direction alone (two
 // per SM moved no more: 210.3 against 210.4 GB/s for a 32-layer burst).
 // Beside compute the count matters: with a bf16 GEMM loop running, a burst of
 // two CTAs per SM cost the GEMM 59-64 % of its throughput during the burst,
-// one per SM 27-34 %, at the same transfer speed.  Two per SM only pays when
-// a backup and a load-back share the link (duplex: 315 against 263 GB/s); a
-// caller that runs them concurrently can ask for it with opts.max_ctas.  The
-// staged path's gather and scatter row kernels (between the device pool and
-// HBM staging, overlapped with copy-engine DMA) take two; with four the
-// staged backup measured slower (139 against 169 GB/s).
+// one per SM 26-34 %, at the same transfer speed.  A load (host to device)
+// defaults to one CTA per two SMs, which takes the deep tasks: it still moved
+// 210-211 GB/s on every benchmark workload, and cost the GEMM 17-27 %.  A
+// backup keeps one CTA per SM: with the deep tasks at one per two SMs a
+// Llama-3-8B backup moved 190.7 against 193.3 GB/s.  Two per SM only pays
+// when a backup and a load-back share the link (duplex); a caller that runs
+// them concurrently can ask for it with opts.max_ctas.  The staged path's
+// gather and scatter row kernels (between the device pool and HBM staging,
+// overlapped with copy-engine DMA) take two per SM.
 constexpr int kCtasPerSmToHost = 1;
-constexpr int kCtasPerSmFromHost = 1;
+constexpr int kSmsPerCtaFromHost = 2;
 constexpr int kCtasPerSmHbm = 2;
 
 struct LaunchCfg {
@@ -195,8 +208,9 @@ SideSpec host_side(const std::vector<PoolInfo>& pools);
 // 16-byte chunks are usable for pool `pi` against paged-side bases `paged_bases`
 // whose layer blocks are `layer_stride` bytes apart.
 bool vec16_ok(const PoolInfo& pi, const std::vector<char*>& paged_bases, int64_t layer_stride);
+// task_bytes: kTaskBytes, or kTaskBytesDeep for a launch of deep tasks.
 void fill_geometry(const PoolInfo& pi, int64_t npairs, int vec, int64_t paged_page_stride,
-                   int64_t paged_tokens, int32_t rows_per_page, PoolGeom* g);
+                   int64_t paged_tokens, int32_t rows_per_page, int64_t task_bytes, PoolGeom* g);
 // Moves pairs [pair_begin, pair_begin + npairs) for layers [layer_begin, layer_end)
 // of every pool and tensor between the device buffers and `side`.  With
 // `signal` (words of a single-launch burst: done and flag indexed by group

@@ -102,9 +102,10 @@ __device__ __forceinline__ void copy_chunks(const longlong2* offs, const char* s
 // Copies the rows of one warp task and returns the task's launch-relative
 // segment.  Called by all 32 lanes of a warp; offs is the warp's table of
 // kMaxRowsPerTask entries in shared memory.
-template <typename IdxT, int MAXSEG, bool LAYER_ROWS, bool DEEP4>
+template <typename IdxT, int MAXSEG, bool LAYER_ROWS, bool DEEP4, bool DEEP>
 __device__ __forceinline__ int copy_task(const CopyParams<MAXSEG>& p, int64_t task, int lane,
                                          longlong2* offs) {
+  constexpr int kU16 = DEEP ? kUnrollDeep : kUnroll;  // 16-byte chunks in flight per lane
   // segment of this task: last s with seg_task_begin[s] <= task
   int lo = 0, hi = p.nseg - 1;
   while (lo < hi) {
@@ -157,7 +158,7 @@ __device__ __forceinline__ int copy_task(const CopyParams<MAXSEG>& p, int64_t ta
     const uint32_t total = uint32_t(nr) * g.cpr;
     // 4-byte chunks keep four times as many in flight, so that a lane has as
     // many bytes outstanding on the host link as with 16-byte chunks
-    if (g.vec == 16) copy_chunks<uint4, 16>(offs, sg.dev, sg.paged, g, 0, total, lane);
+    if (g.vec == 16) copy_chunks<uint4, 16, kU16>(offs, sg.dev, sg.paged, g, 0, total, lane);
     else copy_chunks<uint32_t, 4, 4 * kUnroll>(offs, sg.dev, sg.paged, g, 0, total, lane);
     __syncwarp();  // the table is rewritten by the next task
     return lo;
@@ -220,7 +221,7 @@ __device__ __forceinline__ int copy_task(const CopyParams<MAXSEG>& p, int64_t ta
   __syncwarp();
   const char* src = p.dir == kDevToPaged ? sg.dev : sg.paged;
   char* dst = p.dir == kDevToPaged ? sg.paged : sg.dev;
-  if (g.vec == 16) copy_chunks<uint4, 16>(offs, src, dst, g, chunk0, total, lane);
+  if (g.vec == 16) copy_chunks<uint4, 16, kU16>(offs, src, dst, g, chunk0, total, lane);
   else copy_chunks<uint32_t, 4, DEEP4 ? 4 * kUnroll : kUnroll>(offs, src, dst, g, chunk0, total, lane);
   __syncwarp();  // the table is rewritten by the next task
   return lo;
@@ -231,7 +232,9 @@ __device__ __forceinline__ int copy_task(const CopyParams<MAXSEG>& p, int64_t ta
 // DEEP4: the launch has a pool that takes 4-byte chunks; they run four times
 // as deep, so that a lane keeps as many bytes in flight as with 16-byte
 // chunks.  Launches of 16-byte chunks only compile with the shallow loop.
-template <typename IdxT, int MAXSEG, bool SIGNAL, bool LAYER_ROWS, bool DEEP4>
+// DEEP: deep tasks (about 4 KiB, kUnrollDeep 16-byte chunks in flight per
+// lane) for launches with few CTAs against the host pool.
+template <typename IdxT, int MAXSEG, bool SIGNAL, bool LAYER_ROWS, bool DEEP4, bool DEEP>
 __global__ void __launch_bounds__(kThreadsPerCta)
     row_copy_kernel(const __grid_constant__ CopyParams<MAXSEG> p) {
   __shared__ longlong2 row_offs[kWarpsPerCta][kMaxRowsPerTask];
@@ -243,7 +246,7 @@ __global__ void __launch_bounds__(kThreadsPerCta)
     const int64_t warps_total = int64_t(gridDim.x) * kWarpsPerCta;
     for (int64_t task = int64_t(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5); task < ntasks;
          task += warps_total)
-      copy_task<IdxT, MAXSEG, LAYER_ROWS, DEEP4>(p, task, lane, offs);
+      copy_task<IdxT, MAXSEG, LAYER_ROWS, DEEP4, DEEP>(p, task, lane, offs);
   } else {
     // Tasks are handed out in strict order from one counter, so every task of
     // layer l is taken before any task of layer l+1 and a layer can only wait
@@ -257,7 +260,8 @@ __global__ void __launch_bounds__(kThreadsPerCta)
     int64_t task = __shfl_sync(0xffffffffu, claim, 0);
     while (task < ntasks) {
       claim = lane == 0 ? atomicAdd(next, 1u) : 0u;
-      const int layer = copy_task<IdxT, MAXSEG, false, DEEP4>(p, task, lane, offs) / p.sig.segs_per_layer;
+      const int layer =
+          copy_task<IdxT, MAXSEG, false, DEEP4, DEEP>(p, task, lane, offs) / p.sig.segs_per_layer;
       const int group = (p.sig.layer_base + layer) / lpg;
       if (group != cur_group) {
         if (pending != 0) flush_group(p, cur_group, pending, lane);

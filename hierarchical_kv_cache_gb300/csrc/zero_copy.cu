@@ -39,13 +39,19 @@ hicache_status cuda_fail(cudaError_t e, const char* what) {
                                  cudaGetErrorString(e) + ")");
 }
 
+// CTAs a launch may use: the caller's cap, else the direction's default.
+int cta_budget(const LaunchCfg& cfg, Dir dir) {
+  if (cfg.max_ctas > 0) return cfg.max_ctas;
+  const int sms = device_sm_count();
+  if (cfg.paged_in_hbm) return sms * kCtasPerSmHbm;
+  return dir == kDevToPaged ? sms * kCtasPerSmToHost : std::max(1, sms / kSmsPerCtaFromHost);
+}
+
 template <int MAXSEG, bool SIGNAL>
 hicache_status launch_segments(const CopyParams<MAXSEG>& prm, int32_t index_bits, int64_t ntasks,
-                               const LaunchCfg& cfg, cudaStream_t stream) {
+                               const LaunchCfg& cfg, bool deep, cudaStream_t stream) {
   if (ntasks <= 0) return HICACHE_OK;
-  const int per_sm = cfg.paged_in_hbm ? kCtasPerSmHbm
-                     : prm.dir == kDevToPaged ? kCtasPerSmToHost : kCtasPerSmFromHost;
-  const int max_ctas = cfg.max_ctas > 0 ? cfg.max_ctas : device_sm_count() * per_sm;
+  const int max_ctas = cta_budget(cfg, static_cast<Dir>(prm.dir));
   const int64_t want = (ntasks + kWarpsPerCta - 1) / kWarpsPerCta;
   const int grid = int(std::max<int64_t>(1, std::min<int64_t>(want, max_ctas)));
   bool layer_rows = false, deep4 = false;
@@ -53,11 +59,15 @@ hicache_status launch_segments(const CopyParams<MAXSEG>& prm, int32_t index_bits
     layer_rows = layer_rows || prm.pool[p].layer_rows;
     deep4 = deep4 || prm.pool[p].vec == 4;
   }
-  // one instance per index width, signalling, layer rows and 4-byte chunks
+  // one instance per index width, signalling, layer rows, 4-byte chunks and
+  // task depth
   auto go = [&](auto idx_tag, auto lr_tag, auto d4_tag) {
     using IdxT = decltype(idx_tag);
-    row_copy_kernel<IdxT, MAXSEG, SIGNAL, decltype(lr_tag)::value, decltype(d4_tag)::value>
-        <<<grid, kThreadsPerCta, 0, stream>>>(prm);
+    constexpr bool LR = decltype(lr_tag)::value, D4 = decltype(d4_tag)::value;
+    if (deep)
+      row_copy_kernel<IdxT, MAXSEG, SIGNAL, LR, D4, true><<<grid, kThreadsPerCta, 0, stream>>>(prm);
+    else
+      row_copy_kernel<IdxT, MAXSEG, SIGNAL, LR, D4, false><<<grid, kThreadsPerCta, 0, stream>>>(prm);
   };
   using F = std::false_type;
   using T = std::true_type;
@@ -88,7 +98,10 @@ std::atomic<int64_t> g_launches{0};
 template <typename IdxT, int MAXSEG, bool LAYER_ROWS, bool DEEP4>
 cudaError_t load_static_instance() {
   cudaFuncAttributes a{};
-  return cudaFuncGetAttributes(&a, row_copy_kernel<IdxT, MAXSEG, false, LAYER_ROWS, DEEP4>);
+  cudaError_t e = cudaFuncGetAttributes(&a, row_copy_kernel<IdxT, MAXSEG, false, LAYER_ROWS, DEEP4, false>);
+  if (e == cudaSuccess)
+    e = cudaFuncGetAttributes(&a, row_copy_kernel<IdxT, MAXSEG, false, LAYER_ROWS, DEEP4, true>);
+  return e;
 }
 
 template <typename IdxT, int MAXSEG>
@@ -165,7 +178,7 @@ bool vec16_ok(const PoolInfo& pi, const std::vector<char*>& paged_bases, int64_t
 }
 
 void fill_geometry(const PoolInfo& pi, int64_t npairs, int vec, int64_t paged_page_stride,
-                   int64_t paged_tokens, int32_t rows_per_page, PoolGeom* g) {
+                   int64_t paged_tokens, int32_t rows_per_page, int64_t task_bytes, PoolGeom* g) {
   const int64_t R = moved_row_bytes(pi);
   const bool page_rows = moves_page_rows(pi);
   g->row_bytes = R;
@@ -182,21 +195,22 @@ void fill_geometry(const PoolInfo& pi, int64_t npairs, int vec, int64_t paged_pa
   g->r32 = 32u % g->cpr;
   g->qS = uint32_t(32 * kUnroll) / g->cpr;
   g->rS = uint32_t(32 * kUnroll) % g->cpr;
-  // about kTaskBytes per task: 128 rows of 16 B, one row of 2 KiB, or one
-  // 2 KiB part of a longer row (a state slot of several MiB, a long page row).
+  // about task_bytes per task (2 KiB, or 4 KiB for deep tasks): 128 rows of
+  // 16 B, one row of 2 KiB, or one 2 KiB part of a longer row (a state slot of
+  // several MiB, a long page row).
   // The row count is rounded up so that a task spans whole 128-byte lines when
   // its rows are contiguous (a run of whole pages starts on a line): a line
   // that two warps write at different times reaches the host in two partial
   // writes.  Rows whose bytes already fill lines (2 KiB, 1152 B) keep their count.
-  int64_t rpt = (kTaskBytes + R - 1) / R;
-  if (R <= kTaskBytes) {
+  int64_t rpt = (task_bytes + R - 1) / R;
+  if (R <= task_bytes) {
     const int64_t line_rows = 128 / std::gcd(R, int64_t(128));  // rows that fill whole lines
     const int64_t rounded = (rpt + line_rows - 1) / line_rows * line_rows;
     if (rounded <= kMaxRowsPerTask) rpt = rounded;
   }
   g->rows_per_task = int32_t(std::min<int64_t>(kMaxRowsPerTask, std::max<int64_t>(1, rpt)));
-  g->part_chunks = uint32_t(kTaskBytes / vec);
-  g->parts_per_row = R > kTaskBytes ? int32_t((g->cpr + g->part_chunks - 1) / g->part_chunks) : 1;
+  g->part_chunks = uint32_t(task_bytes / vec);
+  g->parts_per_row = R > task_bytes ? int32_t((g->cpr + g->part_chunks - 1) / g->part_chunks) : 1;
   g->tasks_per_seg = g->parts_per_row > 1
                          ? g->nrows * g->parts_per_row
                          : (g->nrows + g->rows_per_task - 1) / g->rows_per_task;
@@ -218,6 +232,9 @@ hicache_status launch_rows(const std::vector<PoolInfo>& pools, const SideSpec& s
   const bool small =
       !signal && int64_t(layer_end - layer_begin) * segs_per_layer <= kMaxSegSmall;
 
+  // Deep tasks for a launch against the host pool with few CTAs.
+  const bool deep = !cfg.paged_in_hbm && cta_budget(cfg, dir) <= kDeepMaxCtas;
+  const int64_t task_bytes = deep ? kTaskBytesDeep : kTaskBytes;
   auto run = [&](auto& prm, int maxseg) -> hicache_status {
     prm.dev_idx = dev_idx;
     prm.paged_idx = paged_idx;
@@ -230,7 +247,7 @@ hicache_status launch_rows(const std::vector<PoolInfo>& pools, const SideSpec& s
       const PoolInfo& pi = pools[p];
       PoolGeom& g = prm.pool[p];
       fill_geometry(pi, npairs, side.vec16[p] ? 16 : 4, side.page_stride[p],
-                    side.paged_tokens[p], side.rows_per_page[p], &g);
+                    side.paged_tokens[p], side.rows_per_page[p], task_bytes, &g);
       // An all-layer backup into a token-major host pool whose rows do not fill
       // whole lines: one task per token and up to kMaxRowsPerTask of its
       // layers, which are adjacent on the host, instead of rows of one layer
@@ -239,15 +256,15 @@ hicache_status launch_rows(const std::vector<PoolInfo>& pools, const SideSpec& s
       if (dir == kDevToPaged && !signal && !cfg.paged_in_hbm && one_launch &&
           layer_begin == 0 && layer_end == pi.L && !moves_page_rows(pi) &&
           side.rows_per_page[p] == 1 && side.layer_stride[p] == R &&
-          side.page_stride[p] == int64_t(pi.L) * R && R <= kTaskBytes && R % 128 != 0) {
+          side.page_stride[p] == int64_t(pi.L) * R && R <= task_bytes && R % 128 != 0) {
         g.layer_rows = 1;
         g.num_layers = pi.L;
         g.seg_stride = segs_per_layer;
-        // about kTaskBytes of adjacent host rows per task: several tokens when
+        // about task_bytes of adjacent host rows per task: several tokens when
         // a token's layers hold less, part of a token when it has more than
         // kMaxRowsPerTask layers
         const int64_t per_token = int64_t(pi.L) * R;
-        const int64_t kt = std::min<int64_t>(std::max<int64_t>(1, (kTaskBytes + per_token - 1) / per_token),
+        const int64_t kt = std::min<int64_t>(std::max<int64_t>(1, (task_bytes + per_token - 1) / per_token),
                                              std::max<int64_t>(1, kMaxRowsPerTask / pi.L));
         g.tokens_per_task = int32_t(kt);
         g.rows_per_task = pi.L >= kMaxRowsPerTask ? kMaxRowsPerTask : int32_t(kt) * pi.L;
@@ -284,10 +301,10 @@ hicache_status launch_rows(const std::vector<PoolInfo>& pools, const SideSpec& s
         prm.sig.layers_per_group = lpg;
         prm.sig.burst_layers = layer_end - layer_begin;
         st = launch_segments<std::remove_reference_t<decltype(prm)>::kMaxSeg, true>(
-            prm, index_bits, tasks, cfg, stream);
+            prm, index_bits, tasks, cfg, deep, stream);
       } else {
         st = launch_segments<std::remove_reference_t<decltype(prm)>::kMaxSeg, false>(
-            prm, index_bits, tasks, cfg, stream);
+            prm, index_bits, tasks, cfg, deep, stream);
       }
       nseg = 0;
       tasks = 0;

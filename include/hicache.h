@@ -146,13 +146,15 @@ typedef struct hicache_pool {
 typedef struct hicache_opts {
   int32_t path;            /* hicache_path */
   int32_t index_location;  /* hicache_index_location */
-  int32_t max_ctas;        /* 0 = library default (one 256-thread CTA per SM for the host-link
-                              copies); else caps the CTAs of each copy kernel, so that compute
-                              running at the same time keeps the other SMs.  Measured on GB300
-                              beside a bf16 GEMM loop: 38 CTAs still moved 142-171 GB/s and cost
-                              the GEMM 6-17 % of its throughput, against 27-34 % with the
-                              default.  Below HICACHE_AUTO_STAGED_BELOW_CTAS_* the AUTO path may
-                              switch to the staged path (see hicache_auto_path). */
+  int32_t max_ctas;        /* 0 = library default (for the host-link copies, one 256-thread CTA
+                              per SM for a backup, one per two SMs for a load); else caps the
+                              CTAs of each copy kernel, so that compute running at the same
+                              time keeps the other SMs.  Copies of up to 76 CTAs against the
+                              host pool take deep tasks (twice the bytes in flight per warp).
+                              Measured on GB300 beside a bf16 GEMM loop: 32 CTAs moved 169-200
+                              GB/s and cost the GEMM 8-20 % of its throughput, against 21-34 %
+                              with one CTA per SM.  Below HICACHE_AUTO_STAGED_BELOW_CTAS_* the
+                              AUTO path may switch to the staged path (see hicache_auto_path). */
   int32_t reserved;        /* must be 0 */
   void* staging[2];        /* staged path: two device buffers used alternately, 16-byte aligned */
   size_t staging_bytes;    /* bytes of each staging buffer */
@@ -299,8 +301,8 @@ hicache_status hicache_backup_all_layers_static_staging(const hicache_pool* pool
 
 /* Copy-CTA budgets (opts->max_ctas) below which HICACHE_PATH_AUTO takes the
  * staged path when it may (see hicache_auto_path), per direction. */
-#define HICACHE_AUTO_STAGED_BELOW_CTAS_BACKUP 32
-#define HICACHE_AUTO_STAGED_BELOW_CTAS_LOAD 32
+#define HICACHE_AUTO_STAGED_BELOW_CTAS_BACKUP 24
+#define HICACHE_AUTO_STAGED_BELOW_CTAS_LOAD 24
 
 /*
  * The path a call with opts->path == HICACHE_PATH_AUTO takes (host only; no

@@ -2,7 +2,8 @@
 
 The pools have the benchmark's sizes and the transfers run in the benchmark's
 launch configuration: device-located indices, the single-launch burst and the
-default grids.  The oracle then runs on whole-pool images taken before the
+default grids; the 78-layer workload runs once more with 16 CTAs per launch,
+which take the deep tasks.  The oracle then runs on whole-pool images taken before the
 transfers, with the workload's own pair lists (no renumbering), and every byte
 of both pools is compared, touched and untouched: the host pools after the
 backup, the device pools after the load-back burst.  The load-back check feeds
@@ -33,7 +34,7 @@ def _built():
     assert torch.cuda.is_available(), "GPU tests need a CUDA device"
 
 
-def _run_full_size(wl):
+def _run_full_size(wl, max_ctas=0):
     shapes = wl.pools
     P = shapes[0].page_size
     L = shapes[0].num_layers
@@ -56,7 +57,8 @@ def _run_full_size(wl):
 
     words = torch.zeros(4 * L, dtype=torch.int32, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    opts = hk.Opts(index_location=hk.HICACHE_INDEX_DEVICE, burst_words=words, device_error=err)
+    opts = hk.Opts(index_location=hk.HICACHE_INDEX_DEVICE, burst_words=words, device_error=err,
+                   max_ctas=max_ctas)
     events = [torch.cuda.Event() for _ in range(L)]
     dt, ht = G.index_tensors(d, h, "device")
     d2t, _ = G.index_tensors(d2, h, "device")
@@ -84,6 +86,11 @@ def test_dsv3_mla_full_size():
 
 def test_mla78_two_pools_full_size():
     _run_full_size(W.mla78_dsa())
+
+
+def test_mla78_two_pools_full_size_deep_tasks():
+    # 16 CTAs per launch: the deep tasks (4 KiB, 8 chunks in flight per lane)
+    _run_full_size(W.mla78_dsa(), max_ctas=16)
 
 
 def test_mamba_state_pools_full_size():

@@ -179,35 +179,49 @@ def test_staged_burst_with_burst_words(case):
     Its first layers (one in eight) are read zero-copy: layer 0 with a launch of
     its own, the others as one signalling launch whose events a library stream
     records.  The groups after them go through staging.  The events are checked
-    to be recorded by the call, behind a sleep on the caller's stream.
+    to be recorded by the call, behind a sleep on the caller's stream.  The
+    78-layer burst must also stay within a small number of kernel launches:
+    one scatter per staging chunk and one zero-copy launch per pool kind and
+    layer group, not one launch per layer (beside a kernel that holds the SMs
+    every launch waits for room).
     """
     if case == "latent_and_indexer_78_layers":
         lat = G.shape("lat", L=78, T=1, head_num=1, head_dim=576, dtype_size=2, P=64,
                       slots=64 * 48, pages=48)
         idx = G.shape("idx", L=78, T=1, head_num=1, head_dim=132, dtype_size=1, P=64,
                       slots=64 * 48, pages=48, page_granular=True, value_kind="uint8_uniform")
-        shapes, pages = [lat, idx], 20
+        shapes, pages, staging_mib = [lat, idx], 40, 64
     else:
-        shapes, pages = [G.shape("mha", L=24, T=2, head_num=2, head_dim=64, dtype_size=2, P=16,
-                                 slots=16 * 96, pages=64)], 30
+        shapes, pages, staging_mib = [G.shape("mha", L=24, T=2, head_num=2, head_dim=64,
+                                              dtype_size=2, P=16, slots=16 * 96, pages=64)], 30, 16
     pools = [G.make_pool(s, 60 + k) for k, s in enumerate(shapes)]
     s0 = shapes[0]
     L, P = s0.num_layers, s0.page_size
     d, h, _, _ = W.page_pairs(61, pages, s0.device_slots // P, s0.host_pages, P)
     dt, ht = G.index_tensors(d, h, "host")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    opts = _opts(hk.HICACHE_PATH_STAGED, "host", staging=_staging(16 << 20),
+    opts = _opts(hk.HICACHE_PATH_STAGED, "host", staging=_staging(staging_mib << 20),
                  burst_words=_burst_words(L), device_error=err)
+    # a first call in a fresh process loads the kernels it launches, which can
+    # take longer than the sleep the events are armed behind
+    hk.hicache_load_burst(pools, 0, L, ht, dt, opts=opts)
+    torch.cuda.synchronize()
     dev0 = [G.device_images(p) for p in pools]
     host0 = [G.host_images(p) for p in pools]
     events = [torch.cuda.Event() for _ in range(L)]
     _arm(events)
+    before = hk.kernel_launches()
     hk.hicache_load_burst(pools, 0, L, ht, dt, opts=opts, layer_done=events)
+    launches = hk.kernel_launches() - before
     _assert_recorded_behind_sleep(events)
     assert int(err.item()) == 0
     for p, dv, hs in zip(pools, dev0, host0):
         G.oracle_load(p, dv, hs, range(L), h, d)
         G.assert_device_equal(p, dv, f"{case}: staged burst with burst_words")
+    if L == 78:
+        # layer 0, one signalling launch for layers 1-9, then four layer groups
+        # (4, 16, 28, 20 layers) of one or two chunks each: 15 launches
+        assert launches <= 20, f"{launches} kernel launches for one staged burst"
 
 
 # ------------------------------------------------------ ragged shapes and tails
@@ -225,7 +239,9 @@ CASES = [
 
 @pytest.mark.parametrize("case", CASES, ids=[f"R{c[2]*c[3]*c[4]}_P{c[5]}_n{c[8]}" for c in CASES])
 @pytest.mark.parametrize("where", ["device", "host"])
-def test_ragged_backup_and_load(case, where):
+@pytest.mark.parametrize("ctas", [0, 16])
+def test_ragged_backup_and_load(case, where, ctas):
+    """ctas 16: launches of 16 CTAs, which take the deep tasks (about 4 KiB each)."""
     L, T, hn, hd, ds, P, slots, pages, n, frag = case
     s = G.shape(L=L, T=T, head_num=hn, head_dim=hd, dtype_size=ds, P=P, slots=slots, pages=pages)
     pool = G.make_pool(s, seed=n)
@@ -235,7 +251,8 @@ def test_ragged_backup_and_load(case, where):
     d[g.integers(0, n, size=n // 7)] = d[0]  # backup sources may repeat
     dev0, host0 = G.device_images(pool), G.host_images(pool)
     dt, ht = G.index_tensors(d, h, where)
-    hk.hicache_backup_all_layers(pool, dt, ht, opts=_opts(hk.HICACHE_PATH_ZERO_COPY, where))
+    hk.hicache_backup_all_layers(pool, dt, ht,
+                                 opts=_opts(hk.HICACHE_PATH_ZERO_COPY, where, max_ctas=ctas))
     torch.cuda.synchronize()
     G.oracle_backup(pool, dev0, host0, d, h)
     G.assert_host_equal(pool, host0, "backup")
@@ -246,7 +263,8 @@ def test_ragged_backup_and_load(case, where):
     dev1 = G.device_images(pool)
     d2t, h2t = G.index_tensors(d2, h2, where)
     for l in (L - 1, 0):
-        hk.hicache_load_layer(pool, l, h2t, d2t, opts=_opts(hk.HICACHE_PATH_ZERO_COPY, where))
+        hk.hicache_load_layer(pool, l, h2t, d2t,
+                              opts=_opts(hk.HICACHE_PATH_ZERO_COPY, where, max_ctas=ctas))
     torch.cuda.synchronize()
     G.oracle_load(pool, dev1, host0, (L - 1, 0), h2, d2)
     G.assert_device_equal(pool, dev1, "load")
@@ -437,9 +455,11 @@ LAYER_ROW_CASES = [
 @pytest.mark.parametrize("where", ["device", "host"])
 @pytest.mark.parametrize("dtype", [torch.int32, torch.int64])
 @pytest.mark.parametrize("order", ["as_allocated", "falling_addresses"])
-def test_token_major_backup_by_layer_rows(case, where, dtype, order):
+@pytest.mark.parametrize("ctas", [0, 16])
+def test_token_major_backup_by_layer_rows(case, where, dtype, order, ctas):
     """falling_addresses: each tensor's layer buffers sorted so that layer 0 has the
-    highest address, which makes every layer's offset from layer 0 negative."""
+    highest address, which makes every layer's offset from layer 0 negative.  ctas 16:
+    launches of 16 CTAs, which take the deep tasks (about 4 KiB of a token's layers)."""
     import dataclasses
 
     L, T, hn, hd, ds = case
@@ -458,7 +478,7 @@ def test_token_major_backup_by_layer_rows(case, where, dtype, order):
     dt, ht = G.index_tensors(d, h, where, dtype)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     hk.hicache_backup_all_layers(pool, dt, ht, opts=_opts(hk.HICACHE_PATH_ZERO_COPY, where,
-                                                          device_error=err))
+                                                          device_error=err, max_ctas=ctas))
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     G.oracle_backup(pool, dev0, host0, d, h)
