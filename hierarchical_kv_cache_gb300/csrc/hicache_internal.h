@@ -173,9 +173,11 @@ hicache_status plan_runs(const void* dev_idx, const void* host_idx, int32_t inde
 // defaults to one CTA per two SMs, which takes the deep tasks: it still moved
 // 210-211 GB/s on every benchmark workload, and cost the GEMM 17-27 %.  A
 // backup keeps one CTA per SM: with the deep tasks at one per two SMs a
-// Llama-3-8B backup moved 190.7 against 193.3 GB/s.  Two per SM only pays
-// when a backup and a load-back share the link (duplex); a caller that runs
-// them concurrently can ask for it with opts.max_ctas.  The staged path's
+// Llama-3-8B backup moved 190.7 against 193.3 GB/s (a 78-layer one 189.1
+// against 192.4 in another run).  A caller that runs a backup and a load-back
+// at once gets the most from the shared link with 76 deep CTAs on both sides
+// (opts.max_ctas = 76: 298-317 GB/s together, against 245 with the defaults
+// and 240 with two CTAs per SM each).  The staged path's
 // gather and scatter row kernels (between the device pool and HBM staging,
 // overlapped with copy-engine DMA) take two per SM.
 constexpr int kCtasPerSmToHost = 1;

@@ -153,8 +153,11 @@ typedef struct hicache_opts {
                               host pool take deep tasks (twice the bytes in flight per warp).
                               Measured on GB300 beside a bf16 GEMM loop: 32 CTAs moved 169-200
                               GB/s and cost the GEMM 8-20 % of its throughput, against 21-34 %
-                              with one CTA per SM.  Below HICACHE_AUTO_STAGED_BELOW_CTAS_* the
-                              AUTO path may switch to the staged path (see hicache_auto_path). */
+                              with one CTA per SM.  A backup and a load-back running at the
+                              same time moved the most together with 76 on both calls (298-317
+                              GB/s, against about 245 with the defaults).  Below
+                              HICACHE_AUTO_STAGED_BELOW_CTAS_* the AUTO path may switch to the
+                              staged path (see hicache_auto_path). */
   int32_t reserved;        /* must be 0 */
   void* staging[2];        /* staged path: two device buffers used alternately, 16-byte aligned */
   size_t staging_bytes;    /* bytes of each staging buffer */
