@@ -39,6 +39,7 @@ struct StagedRes {
   cudaStream_t copy = nullptr;
   cudaStream_t side = nullptr;  // zero-copy share of a staged call
   cudaEvent_t fork = nullptr, join = nullptr, side_done = nullptr, group_start = nullptr;
+  cudaEvent_t layer0_done = nullptr, zc_done = nullptr;  // a staged load's zero-copy layers
   cudaEvent_t ready[2] = {nullptr, nullptr};
   cudaEvent_t freed[2] = {nullptr, nullptr};
 };
@@ -52,8 +53,8 @@ hicache_status get_res(StagedRes** out) {
   if (!r.init) {
     HK_CUDA(cudaStreamCreateWithFlags(&r.copy, cudaStreamNonBlocking), "cudaStreamCreate(copy)");
     HK_CUDA(cudaStreamCreateWithFlags(&r.side, cudaStreamNonBlocking), "cudaStreamCreate(side)");
-    cudaEvent_t* evs[8] = {&r.fork,     &r.join,     &r.side_done, &r.ready[0],
-                           &r.ready[1], &r.freed[0], &r.freed[1], &r.group_start};
+    cudaEvent_t* evs[10] = {&r.fork,     &r.join,     &r.side_done,   &r.ready[0], &r.ready[1],
+                            &r.freed[0], &r.freed[1], &r.group_start, &r.layer0_done, &r.zc_done};
     for (cudaEvent_t* e : evs) HK_CUDA(cudaEventCreateWithFlags(e, cudaEventDisableTiming), "cudaEventCreate");
     r.init = true;
   }
@@ -362,13 +363,14 @@ hicache_status staged_load(const std::vector<PoolInfo>& all_pools, const hicache
     // A failed load joins the copy stream back into `stream` (copies into the
     // staging buffers may still be in flight), and the side stream, and then
     // completes every remaining layer event.
+    cudaError_t e = cudaSuccess;
     if (forked) {
-      cudaError_t e = cudaEventRecord(r->join, forked);
+      e = cudaEventRecord(r->join, forked);
       if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, r->join, 0);
-      if (e == cudaSuccess && side_used) e = cudaEventRecord(r->side_done, r->side);
-      if (e == cudaSuccess && side_used) e = cudaStreamWaitEvent(stream, r->side_done, 0);
-      if (e != cudaSuccess && s == HICACHE_OK) s = cuda_fail(e, "staged load join");
     }
+    if (e == cudaSuccess && side_used) e = cudaEventRecord(r->side_done, r->side);
+    if (e == cudaSuccess && side_used) e = cudaStreamWaitEvent(stream, r->side_done, 0);
+    if (e != cudaSuccess && s == HICACHE_OK) s = cuda_fail(e, "staged load join");
     for (int32_t i = recorded; i < count; ++i)
       if (layer_done && layer_done[i]) cudaEventRecord(layer_done[i], stream);
     return s;
@@ -418,31 +420,42 @@ hicache_status staged_load(const std::vector<PoolInfo>& all_pools, const hicache
   // of their time.
   const int32_t zc_layers =
       count >= 2 ? int32_t(std::max<int64_t>(1, (count + kZeroCopyShare - 1) / kZeroCopyShare)) : 0;
+  // The zero-copy layers run on the side stream, so that the scatters of the
+  // first layer groups (on `stream`) do not queue behind them and the copy
+  // engine's staging buffers keep turning over.  Their events are recorded
+  // on that stream; the first group's events wait for them, so the events
+  // still complete in layer order.
   auto load_direct_layer = [&](int32_t k) {
     const hicache_status s = launch_rows(all_pools, host_side(all_pools), idx.dev_gpu,
                                          idx.host_gpu, idx.bits, 0, idx.n, kPagedToDev, k, k + 1,
-                                         zero_copy, stream);
+                                         zero_copy, r->side);
     if (s != HICACHE_OK) return s;
     if (layer_done && layer_done[k - layer_begin]) {
-      const cudaError_t e = cudaEventRecord(layer_done[k - layer_begin], stream);
+      const cudaError_t e = cudaEventRecord(layer_done[k - layer_begin], r->side);
       if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(layer_done)");
     }
     ++recorded;
     return HICACHE_OK;
   };
+  HK_TRY(cudaEventRecord(r->fork, stream), "cudaEventRecord(fork)");
   if (zc_layers > 0) {
+    HK_TRY(cudaStreamWaitEvent(r->side, r->fork, 0), "cudaStreamWaitEvent(fork)");
+    side_used = true;
     st = load_direct_layer(layer_begin);
     if (st != HICACHE_OK) return finish(st);
+    // the copy engine starts once layer 0 has landed: layer 0 has the link to itself
+    HK_TRY(cudaEventRecord(r->layer0_done, r->side), "cudaEventRecord(layer 0 done)");
+    HK_TRY(cudaStreamWaitEvent(copy, r->layer0_done, 0), "cudaStreamWaitEvent(layer 0 done)");
+  } else {
+    HK_TRY(cudaStreamWaitEvent(copy, r->fork, 0), "cudaStreamWaitEvent(fork)");
   }
-  HK_TRY(cudaEventRecord(r->fork, stream), "cudaEventRecord(fork)");
-  HK_TRY(cudaStreamWaitEvent(copy, r->fork, 0), "cudaStreamWaitEvent(fork)");
   forked = copy;
   if (zc_layers >= 3 && o.burst_words && signaled_burst_available()) {
     // the other zero-copy layers as one signalling launch (fewer launches to
     // wait for SMs when a concurrent kernel holds them); it records their
     // events on every return path
     st = signaled_burst(all_pools, host_side(all_pools), idx, o, layer_begin + 1,
-                        layer_begin + zc_layers, stream, layer_done ? layer_done + 1 : nullptr);
+                        layer_begin + zc_layers, r->side, layer_done ? layer_done + 1 : nullptr);
     recorded += zc_layers - 1;
     if (st != HICACHE_OK) return finish(st);
   } else {
@@ -451,6 +464,8 @@ hicache_status staged_load(const std::vector<PoolInfo>& all_pools, const hicache
       if (st != HICACHE_OK) return finish(st);
     }
   }
+  if (zc_layers > 0) HK_TRY(cudaEventRecord(r->zc_done, r->side), "cudaEventRecord(zero-copy layers done)");
+  bool first_group = true;
   const int32_t first = layer_begin + zc_layers;
   int64_t step = 0;
   // the groups start small whatever the zero-copy share, so that the layer
@@ -530,8 +545,12 @@ hicache_status staged_load(const std::vector<PoolInfo>& all_pools, const hicache
       if (st != HICACHE_OK) return finish(st);
       if (last_chunk) {
         // the group has landed once its zero-copy work has too: its events
+        // (the first group's also come after the zero-copy layers')
         if (group_side)
           HK_TRY(cudaStreamWaitEvent(stream, r->side_done, 0), "cudaStreamWaitEvent(side done)");
+        else if (first_group && zc_layers > 0)
+          HK_TRY(cudaStreamWaitEvent(stream, r->zc_done, 0), "cudaStreamWaitEvent(zero-copy layers)");
+        first_group = false;
         for (int32_t k = l; k < l + g; ++k) {
           if (layer_done && layer_done[k - layer_begin])
             HK_TRY(cudaEventRecord(layer_done[k - layer_begin], stream), "cudaEventRecord(layer_done)");
@@ -540,6 +559,11 @@ hicache_status staged_load(const std::vector<PoolInfo>& all_pools, const hicache
       }
       HK_TRY(cudaEventRecord(r->freed[b], stream), "cudaEventRecord(freed)");
     }
+  }
+  // the side stream's work joins `stream` before the call returns
+  if (side_used) {
+    HK_TRY(cudaEventRecord(r->side_done, r->side), "cudaEventRecord(side done)");
+    HK_TRY(cudaStreamWaitEvent(stream, r->side_done, 0), "cudaStreamWaitEvent(side done)");
   }
 #undef HK_TRY
   return HICACHE_OK;

@@ -229,11 +229,12 @@ hicache_status hicache_load_layer(const hicache_pool* pools, int32_t num_pools, 
  * call returns.  A layer of 2 MiB or more (all pools) is a group of its own;
  * smaller layers form groups of about 2 MiB, whose events are recorded together
  * once the whole group has landed.  The words must not be shared by bursts that overlap on the
- * GPU.  The staged path ignores burst_words.
+ * GPU.
  * The staged path reads the first layers of a burst of two or more layers
- * zero-copy (the SMs read the host pool; one layer in eight, at least one:
- * the first with its own launch and event, the others likewise, or, given
- * opts->burst_words, as one signalling launch), then copies groups of consecutive
+ * zero-copy on a library stream (the SMs read the host pool; one layer in
+ * eight, at least one: the first with its own launch and event, the others
+ * likewise, or, given opts->burst_words, as one signalling launch), then
+ * copies groups of consecutive
  * layers of each host page per DMA, each group four times the previous (up to
  * about 4 MiB per copy, in chunks of pages that fit a staging buffer),
  * scatters each chunk in one launch, and records a group's events once its
