@@ -172,12 +172,18 @@ bool device_pages_consecutive(const void* dev_idx, int32_t bits, int64_t n, int3
 // 659 KB per page) is such a pool beside its 5.75 MB latent pages.
 constexpr int64_t kDirectPageBytes = int64_t(1) << 20;
 
-// A staged call moves this fraction of its work (1 / kZeroCopyShare) zero-copy
-// beside the copy engine: the last pages of a backup; the first layers of a
-// load, and the last pages of each of its layer groups.  The copy engine leaves the link idle for its fixed time per copy
-// (2.4-3.3 us on GB300) and moves a load's first small layer groups at a
+// A staged load moves this fraction of its work (1 / kZeroCopyShare) zero-copy
+// beside the copy engine: its first layers, and the last pages of each of its
+// layer groups.  The copy engine leaves the link idle for its fixed time per
+// copy (2.4-3.3 us on GB300) and moves a load's first small layer groups at a
 // fraction of the link; SM-issued traffic beside it fills those gaps.
 constexpr int64_t kZeroCopyShare = 8;
+// The staged backup moves a larger share, a quarter of its pages, zero-copy:
+// against an eighth it lifted the backup from 172 to 175.5 GB/s (Llama-3-8B,
+// 89.0 to 90.9 % of the link), 180 to 183 (78-layer) and 173 to 176 (DSv3),
+// and under a 16-CTA cap beside a GEMM loop moved more too (Llama 168 against
+// 165, 78-layer 89 against 76 GB/s), at a GEMM cost 2-3 points higher.
+constexpr int64_t kBackupZeroCopyShare = 4;
 
 // Splits a staged call's pools into those that go through staging and the
 // small ones that move zero-copy beside them.
@@ -260,8 +266,10 @@ hicache_status staged_backup(const std::vector<PoolInfo>& all_pools, const hicac
   const LaunchCfg cfg{o.max_ctas, o.device_error, /*paged_in_hbm=*/true};
   const LaunchCfg zero_copy{o.max_ctas, o.device_error, /*paged_in_hbm=*/false};
   const int64_t groups = int64_t(hp.size());
-  // the last pages move zero-copy beside the copy engine (kZeroCopyShare)
-  const int64_t zc_pages = groups >= kZeroCopyShare ? (groups + kZeroCopyShare - 1) / kZeroCopyShare : 0;
+  // the last pages move zero-copy beside the copy engine (kBackupZeroCopyShare)
+  const int64_t zc_pages = groups >= kBackupZeroCopyShare
+                               ? (groups + kBackupZeroCopyShare - 1) / kBackupZeroCopyShare
+                               : 0;
   const int64_t dma_groups = groups - zc_pages;
   const bool dev_consecutive = device_pages_consecutive(idx.dev_cpu, idx.bits, idx.n, P);
   const SideSpec side[2] = {staging_side(pools, lay, static_cast<char*>(o.staging[0]), L, 0),

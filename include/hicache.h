@@ -244,7 +244,7 @@ hicache_status hicache_load_layer(const hicache_pool* pools, int32_t num_pools, 
  * moves the group's other pages, and so is a pool whose host page is under
  * 1 MiB beside a larger pool (one launch each per group); the group's events
  * also wait for that stream.  The staged backup likewise moves the last
- * eighth of its pages, and such small pools, zero-copy on a library stream
+ * quarter of its pages, and such small pools, zero-copy on a library stream
  * beside its DMAs.
  */
 hicache_status hicache_load_burst(const hicache_pool* pools, int32_t num_pools,

@@ -127,22 +127,23 @@ def test_tiny_mha_backup_then_load(where, dtype, path):
 
 
 # The page counts the pages' unit test probes, then the counts whose staged part
-# (a staged call moves the last eighth of its pages zero-copy) is 63/64/65/128/129
-# for the backup and 95/96/97 for the load.
-@pytest.mark.parametrize("pages", [1, 63, 64, 65, 128, 129, 72, 74, 75, 147, 148, 109, 110, 111])
+# (a staged backup moves the last quarter of its pages zero-copy, a load the
+# last eighth of each layer group's) is 63/64/65/128/129 for the backup and
+# 95/96/97 for the load.
+@pytest.mark.parametrize("pages", [1, 63, 64, 65, 128, 129, 84, 86, 87, 171, 172, 109, 110, 111])
 @pytest.mark.parametrize("path", ["zero_copy", "zero_copy_single_launch", "staged"])
 def test_boundary_page_counts(pages, path):
     """The page counts the pages' unit test probes, through the CUDA path.
 
     The staging buffers hold exactly 64 pages of all layers. A staged backup
-    copies all but the last eighth of its pages through them (72/74/75 pages:
-    63/64/65 staged, 147/148: 128/129), so those fall just inside, on and just
+    copies all but the last quarter of its pages through them (84/86/87 pages:
+    63/64/65 staged, 171/172: 128/129), so those fall just inside, on and just
     past its chunk boundaries. A 3-layer staged load reads its first layer
     zero-copy and copies the other two as one group, in chunks of 96 pages,
     all but the group's last eighth of pages (109/110/111 pages: 95/96/97
     copied).
     """
-    s = G.shape(L=3, T=2, head_num=2, head_dim=64, dtype_size=2, P=16, slots=16 * 300, pages=160)
+    s = G.shape(L=3, T=2, head_num=2, head_dim=64, dtype_size=2, P=16, slots=16 * 360, pages=180)
     pool = G.make_pool(s, seed=40 + pages)
     P = s.page_size
     d, h, dp, _ = W.page_pairs(41 + pages, pages, s.device_slots // P, s.host_pages, P)

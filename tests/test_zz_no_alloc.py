@@ -10,7 +10,7 @@ Checked here:
   - on two calls in a row (the second reuses the array the first one left
     behind), the host pool equals, byte for byte, both the CPU oracle's backup
     of the same pairs and what hicache_backup_all_layers writes;
-  - page counts whose staged part (all but the last eighth of the pages, which
+  - page counts whose staged part (all but the last quarter of the pages, which
     move zero-copy) lies just below, on and just past the 16 MiB half of the
     array, and a list of three chunks, so that one call refills a half it used
     before;
@@ -78,7 +78,7 @@ def _mha_shape():
     # 2 tensors x 8 layers x 64 tokens x 512 B = 512 KiB per host page: exactly 32 pages
     # fill one 16 MiB half of the static array
     return [W.PoolShape("mha", num_layers=8, num_tensors=2, head_num=4, head_dim=128,
-                        dtype_size=1, page_size=64, device_slots=64 * 96, host_pages=80)]
+                        dtype_size=1, page_size=64, device_slots=64 * 128, host_pages=100)]
 
 
 def _mla_dsa_shapes():
@@ -90,13 +90,13 @@ def _mla_dsa_shapes():
     return [lat, idx]
 
 
-# (shapes, pages per call).  The staged backup moves the last ceil(pages / 8) pages
-# zero-copy, so 36 / 37 / 38 pages put 31 / 32 / 33 pages through the array: just
-# below, on and one past a half.  75 pages put 65 through it, three chunks (32 + 32
+# (shapes, pages per call).  The staged backup moves the last ceil(pages / 4) pages
+# zero-copy, so 42 / 43 / 44 pages put 31 / 32 / 33 pages through the array: just
+# below, on and one past a half.  87 pages put 65 through it, three chunks (32 + 32
 # + 1), so the third refills the first half within one call.  The two-pool case has
-# 481.5 KiB pages, 34 per half; 50 pages put 43 through it, over both halves.
-CASES = {"mha36": (_mha_shape, 36), "mha37": (_mha_shape, 37), "mha38": (_mha_shape, 38),
-         "mha75": (_mha_shape, 75), "mla_dsa50": (_mla_dsa_shapes, 50)}
+# 481.5 KiB pages, 34 per half; 50 pages put 37 through it, over both halves.
+CASES = {"mha42": (_mha_shape, 42), "mha43": (_mha_shape, 43), "mha44": (_mha_shape, 44),
+         "mha87": (_mha_shape, 87), "mla_dsa50": (_mla_dsa_shapes, 50)}
 
 
 @pytest.mark.parametrize("case", sorted(CASES))
