@@ -172,18 +172,20 @@ bool device_pages_consecutive(const void* dev_idx, int32_t bits, int64_t n, int3
 // 659 KB per page) is such a pool beside its 5.75 MB latent pages.
 constexpr int64_t kDirectPageBytes = int64_t(1) << 20;
 
-// A staged load moves this fraction of its work (1 / kZeroCopyShare) zero-copy
-// beside the copy engine: its first layers, and the last pages of each of its
-// layer groups.  The copy engine leaves the link idle for its fixed time per
-// copy (2.4-3.3 us on GB300) and moves a load's first small layer groups at a
-// fraction of the link; SM-issued traffic beside it fills those gaps.
-constexpr int64_t kZeroCopyShare = 8;
-// The staged backup moves a larger share, a quarter of its pages, zero-copy:
-// against an eighth it lifted the backup from 172 to 175.5 GB/s (Llama-3-8B,
-// 89.0 to 90.9 % of the link), 180 to 183 (78-layer) and 173 to 176 (DSv3),
-// and under a 16-CTA cap beside a GEMM loop moved more too (Llama 168 against
-// 165, 78-layer 89 against 76 GB/s), at a GEMM cost 2-3 points higher.
-constexpr int64_t kBackupZeroCopyShare = 4;
+// A staged call moves part of its work zero-copy beside the copy engine: the
+// copy engine leaves the link idle for its fixed time per copy (2.4-3.3 us on
+// GB300) and moves a load's first small layer groups at a fraction of the
+// link; SM-issued traffic beside it fills those gaps.
+// - A load's first layers, one in kZeroCopyLayerShare.
+// - The last pages of a backup, and of each layer group of a load, one in
+//   kZeroCopyPageShare.  Against an eighth, a quarter lifted the staged backup
+//   from 172 to 175.5 GB/s (Llama-3-8B, 89.0 to 90.9 % of the link), 180 to
+//   183 (78-layer) and 173 to 176 (DSv3), and the staged burst from 165 to 174
+//   (Llama-3-8B), 169 to 177 (78-layer) and 152 to 161 (DSv3); under a 16-CTA
+//   cap beside a GEMM loop both moved as much or more, at a GEMM cost up to 3
+//   points higher.
+constexpr int64_t kZeroCopyLayerShare = 8;
+constexpr int64_t kZeroCopyPageShare = 4;
 
 // Splits a staged call's pools into those that go through staging and the
 // small ones that move zero-copy beside them.
@@ -266,9 +268,9 @@ hicache_status staged_backup(const std::vector<PoolInfo>& all_pools, const hicac
   const LaunchCfg cfg{o.max_ctas, o.device_error, /*paged_in_hbm=*/true};
   const LaunchCfg zero_copy{o.max_ctas, o.device_error, /*paged_in_hbm=*/false};
   const int64_t groups = int64_t(hp.size());
-  // the last pages move zero-copy beside the copy engine (kBackupZeroCopyShare)
-  const int64_t zc_pages = groups >= kBackupZeroCopyShare
-                               ? (groups + kBackupZeroCopyShare - 1) / kBackupZeroCopyShare
+  // the last pages move zero-copy beside the copy engine (kZeroCopyPageShare)
+  const int64_t zc_pages = groups >= kZeroCopyPageShare
+                               ? (groups + kZeroCopyPageShare - 1) / kZeroCopyPageShare
                                : 0;
   const int64_t dma_groups = groups - zc_pages;
   const bool dev_consecutive = device_pages_consecutive(idx.dev_cpu, idx.bits, idx.n, P);
@@ -400,9 +402,12 @@ hicache_status staged_load(const std::vector<PoolInfo>& all_pools, const hicache
   const LaunchCfg zero_copy{o.max_ctas, o.device_error, /*paged_in_hbm=*/false};
   const int64_t groups = int64_t(hp.size());
   if (groups == 0) return finish(HICACHE_OK);  // nothing to move; the events still fire
-  // The last pages of every layer group (kZeroCopyShare) are read zero-copy
-  // on the side stream while the copy engine moves the group's other pages.
-  const int64_t zc_pages = groups >= kZeroCopyShare ? (groups + kZeroCopyShare - 1) / kZeroCopyShare : 0;
+  // The last pages of every layer group (kZeroCopyPageShare) are read
+  // zero-copy on the side stream while the copy engine moves the group's
+  // other pages.
+  const int64_t zc_pages = groups >= kZeroCopyPageShare
+                               ? (groups + kZeroCopyPageShare - 1) / kZeroCopyPageShare
+                               : 0;
   const int64_t dma_groups = groups - zc_pages;
   const bool group_side = zc_pages > 0 || !direct.empty();  // a group has side-stream work
   const bool dev_consecutive = device_pages_consecutive(idx.dev_cpu, idx.bits, idx.n, P);
@@ -417,7 +422,7 @@ hicache_status staged_load(const std::vector<PoolInfo>& all_pools, const hicache
     if (e_ != cudaSuccess) return finish(cuda_fail(e_, what)); \
   } while (0)
 
-  // The first layers of a burst of two or more (one in kZeroCopyShare, at
+  // The first layers of a burst of two or more (one in kZeroCopyLayerShare, at
   // least one) are read zero-copy: the SMs read the host pool directly, one
   // launch and event per layer.  Through the copy engine the first layer
   // would cost one small copy per host page before its event, and the first
@@ -427,7 +432,8 @@ hicache_status staged_load(const std::vector<PoolInfo>& all_pools, const hicache
   // engine's first, smaller groups, whose copies leave the link idle for part
   // of their time.
   const int32_t zc_layers =
-      count >= 2 ? int32_t(std::max<int64_t>(1, (count + kZeroCopyShare - 1) / kZeroCopyShare)) : 0;
+      count >= 2 ? int32_t(std::max<int64_t>(1, (count + kZeroCopyLayerShare - 1) / kZeroCopyLayerShare))
+                 : 0;
   // The zero-copy layers run on the side stream, so that the scatters of the
   // first layer groups (on `stream`) do not queue behind them and the copy
   // engine's staging buffers keep turning over.  Their events are recorded

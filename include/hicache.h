@@ -239,7 +239,7 @@ hicache_status hicache_load_layer(const hicache_pool* pools, int32_t num_pools, 
  * about 4 MiB per copy, in chunks of pages that fit a staging buffer),
  * scatters each chunk in one launch, and records a group's events once its
  * last chunk has landed.  Its later layer events therefore arrive in groups,
- * each no earlier than its own layer's data.  The last eighth of the pages
+ * each no earlier than its own layer's data.  The last quarter of the pages
  * of each group is read zero-copy on a library stream while the copy engine
  * moves the group's other pages, and so is a pool whose host page is under
  * 1 MiB beside a larger pool (one launch each per group); the group's events

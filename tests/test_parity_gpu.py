@@ -128,9 +128,9 @@ def test_tiny_mha_backup_then_load(where, dtype, path):
 
 # The page counts the pages' unit test probes, then the counts whose staged part
 # (a staged backup moves the last quarter of its pages zero-copy, a load the
-# last eighth of each layer group's) is 63/64/65/128/129 for the backup and
+# last quarter of each layer group's) is 63/64/65/128/129 for the backup and
 # 95/96/97 for the load.
-@pytest.mark.parametrize("pages", [1, 63, 64, 65, 128, 129, 84, 86, 87, 171, 172, 109, 110, 111])
+@pytest.mark.parametrize("pages", [1, 63, 64, 65, 128, 129, 84, 86, 87, 171, 172, 127, 130])
 @pytest.mark.parametrize("path", ["zero_copy", "zero_copy_single_launch", "staged"])
 def test_boundary_page_counts(pages, path):
     """The page counts the pages' unit test probes, through the CUDA path.
@@ -140,7 +140,7 @@ def test_boundary_page_counts(pages, path):
     63/64/65 staged, 171/172: 128/129), so those fall just inside, on and just
     past its chunk boundaries. A 3-layer staged load reads its first layer
     zero-copy and copies the other two as one group, in chunks of 96 pages,
-    all but the group's last eighth of pages (109/110/111 pages: 95/96/97
+    all but the group's last quarter of pages (127/128/130 pages: 95/96/97
     copied).
     """
     s = G.shape(L=3, T=2, head_num=2, head_dim=64, dtype_size=2, P=16, slots=16 * 360, pages=180)
