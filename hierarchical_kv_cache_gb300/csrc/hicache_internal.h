@@ -210,9 +210,11 @@ SideSpec host_side(const std::vector<PoolInfo>& pools);
 // 16-byte chunks are usable for pool `pi` against paged-side bases `paged_bases`
 // whose layer blocks are `layer_stride` bytes apart.
 bool vec16_ok(const PoolInfo& pi, const std::vector<char*>& paged_bases, int64_t layer_stride);
-// task_bytes: kTaskBytes, or kTaskBytesDeep for a launch of deep tasks.
+// task_bytes and unroll16: kTaskBytes and kUnroll, or kTaskBytesDeep and
+// kUnrollDeep for a launch of deep tasks.
 void fill_geometry(const PoolInfo& pi, int64_t npairs, int vec, int64_t paged_page_stride,
-                   int64_t paged_tokens, int32_t rows_per_page, int64_t task_bytes, PoolGeom* g);
+                   int64_t paged_tokens, int32_t rows_per_page, int64_t task_bytes, int unroll16,
+                   PoolGeom* g);
 // Moves pairs [pair_begin, pair_begin + npairs) for layers [layer_begin, layer_end)
 // of every pool and tensor between the device buffers and `side`.  With
 // `signal` (words of a single-launch burst: done and flag indexed by group
