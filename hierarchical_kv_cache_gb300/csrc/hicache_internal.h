@@ -211,10 +211,11 @@ SideSpec host_side(const std::vector<PoolInfo>& pools);
 // whose layer blocks are `layer_stride` bytes apart.
 bool vec16_ok(const PoolInfo& pi, const std::vector<char*>& paged_bases, int64_t layer_stride);
 // task_bytes and unroll16: kTaskBytes and kUnroll, or kTaskBytesDeep and
-// kUnrollDeep for a launch of deep tasks.
+// kUnrollDeep for a launch of deep tasks.  fill_rows: choose the rows per task
+// that fill the copy loop's iterations (else the count nearest task_bytes).
 void fill_geometry(const PoolInfo& pi, int64_t npairs, int vec, int64_t paged_page_stride,
                    int64_t paged_tokens, int32_t rows_per_page, int64_t task_bytes, int unroll16,
-                   PoolGeom* g);
+                   bool fill_rows, PoolGeom* g);
 // Moves pairs [pair_begin, pair_begin + npairs) for layers [layer_begin, layer_end)
 // of every pool and tensor between the device buffers and `side`.  With
 // `signal` (words of a single-launch burst: done and flag indexed by group

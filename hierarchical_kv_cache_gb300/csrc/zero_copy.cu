@@ -179,7 +179,7 @@ bool vec16_ok(const PoolInfo& pi, const std::vector<char*>& paged_bases, int64_t
 
 void fill_geometry(const PoolInfo& pi, int64_t npairs, int vec, int64_t paged_page_stride,
                    int64_t paged_tokens, int32_t rows_per_page, int64_t task_bytes, int unroll16,
-                   PoolGeom* g) {
+                   bool fill_rows, PoolGeom* g) {
   const int64_t R = moved_row_bytes(pi);
   const bool page_rows = moves_page_rows(pi);
   g->row_bytes = R;
@@ -208,7 +208,7 @@ void fill_geometry(const PoolInfo& pi, int64_t npairs, int vec, int64_t paged_pa
     const int64_t line_rows = 128 / std::gcd(R, int64_t(128));  // rows that fill whole lines
     const int64_t rounded = (rpt + line_rows - 1) / line_rows * line_rows;
     if (rounded <= kMaxRowsPerTask) rpt = rounded;
-    if (vec == 16) {
+    if (vec == 16 && fill_rows) {
       // The copy loop moves 32 * unroll16 chunks per iteration, one host-link
       // round trip each.  Among the row counts that keep whole lines and at
       // most two iterations, a count that fills the iterations' chunks better
@@ -257,6 +257,11 @@ hicache_status launch_rows(const std::vector<PoolInfo>& pools, const SideSpec& s
   // Deep tasks for a launch against the host pool with few CTAs.
   const bool deep = !cfg.paged_in_hbm && cta_budget(cfg, dir) <= kDeepMaxCtas;
   const int64_t task_bytes = deep ? kTaskBytesDeep : kTaskBytes;
+  // Rows per task chosen to fill the copy loop's iterations, except for a
+  // load at its default budget: there the link is full either way, and the
+  // larger tasks measured a longer lag for a consumer gated by the layer
+  // events (78-layer: 92 against 57 us after its event).
+  const bool fill_rows = !(deep && cfg.max_ctas <= 0);
   auto run = [&](auto& prm, int maxseg) -> hicache_status {
     prm.dev_idx = dev_idx;
     prm.paged_idx = paged_idx;
@@ -270,7 +275,7 @@ hicache_status launch_rows(const std::vector<PoolInfo>& pools, const SideSpec& s
       PoolGeom& g = prm.pool[p];
       fill_geometry(pi, npairs, side.vec16[p] ? 16 : 4, side.page_stride[p],
                     side.paged_tokens[p], side.rows_per_page[p], task_bytes,
-                    deep ? kUnrollDeep : kUnroll, &g);
+                    deep ? kUnrollDeep : kUnroll, fill_rows, &g);
       // An all-layer backup into a token-major host pool whose rows do not fill
       // whole lines: one task per token and up to kMaxRowsPerTask of its
       // layers, which are adjacent on the host, instead of rows of one layer
