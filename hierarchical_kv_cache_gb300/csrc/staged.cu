@@ -6,10 +6,13 @@
 // the host.  Here the staging is double-buffered so that the gather of chunk
 // k+1 overlaps the link transfer of chunk k, the DMA is one copy per run of
 // consecutive host pages (not one per row), and the same idea serves the
-// per-layer load in reverse (2-D DMA of a group of layer blocks per host page,
-// then a scatter kernel per layer; a burst's first layer is read zero-copy).  The staged path needs the pairs to be whole host pages in
-// groups of page_size (what a page-granular host allocator hands out) and the
-// indices on the host, because the DMA spans are planned on the CPU.
+// per-layer load in reverse (a 2-D DMA of a group of layer blocks per host
+// page, then one scatter launch per chunk of pages; a burst's first layers
+// are read zero-copy).  A share of the pages, and pools too small for DMAs of
+// their own, move zero-copy on a side stream beside the copy engine.  The
+// staged path needs the pairs to be whole host pages in groups of page_size
+// (what a page-granular host allocator hands out) and the indices on the
+// host, because the DMA spans are planned on the CPU.
 #include <cuda_runtime.h>
 
 #include <algorithm>

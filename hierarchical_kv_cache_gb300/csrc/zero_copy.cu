@@ -9,7 +9,8 @@
 // path).
 //
 // Work decomposition: a warp task is about 2 KiB of one segment (one pool,
-// tensor and layer): up to 128 rows, or one 2 KiB part of a longer row.  Lane
+// tensor and layer; 4 KiB for a launch of few CTAs against the host pool):
+// up to 128 rows, or one 2 KiB (4 KiB) part of a longer row.  Lane
 // r loads the pairs of rows r, r + 32, ..., checks them and writes each row's
 // source and destination byte offsets into the warp's table in shared memory.
 // The task's rows are then treated as one flat array of VEC-byte chunks: lane
