@@ -234,17 +234,18 @@ __device__ __forceinline__ int copy_task(const CopyParams<MAXSEG>& p, int64_t ta
 // chunks.  Launches of 16-byte chunks only compile with the shallow loop.
 // DEEP: deep tasks (about 4 KiB, kUnrollDeep 16-byte chunks in flight per
 // lane) for launches with few CTAs against the host pool.
-template <typename IdxT, int MAXSEG, bool SIGNAL, bool LAYER_ROWS, bool DEEP4, bool DEEP>
-__global__ void __launch_bounds__(kThreadsPerCta)
+// WARPS: warps per CTA (kWarpsPerCta, or kWarpsPerCtaWide under a small cap).
+template <typename IdxT, int MAXSEG, bool SIGNAL, bool LAYER_ROWS, bool DEEP4, bool DEEP, int WARPS>
+__global__ void __launch_bounds__(WARPS * 32)
     row_copy_kernel(const __grid_constant__ CopyParams<MAXSEG> p) {
-  __shared__ longlong2 row_offs[kWarpsPerCta][kMaxRowsPerTask];
+  __shared__ longlong2 row_offs[WARPS][kMaxRowsPerTask];
   const int lane = threadIdx.x & 31;
   longlong2* offs = row_offs[threadIdx.x >> 5];
   const int64_t ntasks = p.seg_task_begin[p.nseg];
   if constexpr (!SIGNAL) {
     // Static striding: warp w takes tasks w, w + W, w + 2W, ...
-    const int64_t warps_total = int64_t(gridDim.x) * kWarpsPerCta;
-    for (int64_t task = int64_t(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5); task < ntasks;
+    const int64_t warps_total = int64_t(gridDim.x) * WARPS;
+    for (int64_t task = int64_t(blockIdx.x) * WARPS + (threadIdx.x >> 5); task < ntasks;
          task += warps_total)
       copy_task<IdxT, MAXSEG, LAYER_ROWS, DEEP4, DEEP>(p, task, lane, offs);
   } else {

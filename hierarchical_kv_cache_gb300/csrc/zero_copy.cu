@@ -52,23 +52,35 @@ template <int MAXSEG, bool SIGNAL>
 hicache_status launch_segments(const CopyParams<MAXSEG>& prm, int32_t index_bits, int64_t ntasks,
                                const LaunchCfg& cfg, bool deep, cudaStream_t stream) {
   if (ntasks <= 0) return HICACHE_OK;
-  const int max_ctas = cta_budget(cfg, static_cast<Dir>(prm.dir));
-  const int64_t want = (ntasks + kWarpsPerCta - 1) / kWarpsPerCta;
-  const int grid = int(std::max<int64_t>(1, std::min<int64_t>(want, max_ctas)));
   bool layer_rows = false, deep4 = false;
   for (int p = 0; p < kMaxPools; ++p) {
     layer_rows = layer_rows || prm.pool[p].layer_rows;
     deep4 = deep4 || prm.pool[p].vec == 4;
   }
-  // one instance per index width, signalling, layer rows, 4-byte chunks and
-  // task depth
+  // 16-warp CTAs under a small cap (the layer-row instances keep 8 warps)
+  const bool wide = deep && !layer_rows && cfg.max_ctas > 0 && cfg.max_ctas <= kWideMaxCtas;
+  const int warps = wide ? kWarpsPerCtaWide : kWarpsPerCta;
+  const int max_ctas = cta_budget(cfg, static_cast<Dir>(prm.dir));
+  const int64_t want = (ntasks + warps - 1) / warps;
+  const int grid = int(std::max<int64_t>(1, std::min<int64_t>(want, max_ctas)));
+  // one instance per index width, signalling, layer rows, 4-byte chunks, task
+  // depth and CTA width
   auto go = [&](auto idx_tag, auto lr_tag, auto d4_tag) {
     using IdxT = decltype(idx_tag);
     constexpr bool LR = decltype(lr_tag)::value, D4 = decltype(d4_tag)::value;
+    if constexpr (!LR) {
+      if (wide) {
+        row_copy_kernel<IdxT, MAXSEG, SIGNAL, false, D4, true, kWarpsPerCtaWide>
+            <<<grid, kWarpsPerCtaWide * 32, 0, stream>>>(prm);
+        return;
+      }
+    }
     if (deep)
-      row_copy_kernel<IdxT, MAXSEG, SIGNAL, LR, D4, true><<<grid, kThreadsPerCta, 0, stream>>>(prm);
+      row_copy_kernel<IdxT, MAXSEG, SIGNAL, LR, D4, true, kWarpsPerCta>
+          <<<grid, kThreadsPerCta, 0, stream>>>(prm);
     else
-      row_copy_kernel<IdxT, MAXSEG, SIGNAL, LR, D4, false><<<grid, kThreadsPerCta, 0, stream>>>(prm);
+      row_copy_kernel<IdxT, MAXSEG, SIGNAL, LR, D4, false, kWarpsPerCta>
+          <<<grid, kThreadsPerCta, 0, stream>>>(prm);
   };
   using F = std::false_type;
   using T = std::true_type;
@@ -99,9 +111,16 @@ std::atomic<int64_t> g_launches{0};
 template <typename IdxT, int MAXSEG, bool LAYER_ROWS, bool DEEP4>
 cudaError_t load_static_instance() {
   cudaFuncAttributes a{};
-  cudaError_t e = cudaFuncGetAttributes(&a, row_copy_kernel<IdxT, MAXSEG, false, LAYER_ROWS, DEEP4, false>);
+  cudaError_t e = cudaFuncGetAttributes(
+      &a, row_copy_kernel<IdxT, MAXSEG, false, LAYER_ROWS, DEEP4, false, kWarpsPerCta>);
   if (e == cudaSuccess)
-    e = cudaFuncGetAttributes(&a, row_copy_kernel<IdxT, MAXSEG, false, LAYER_ROWS, DEEP4, true>);
+    e = cudaFuncGetAttributes(
+        &a, row_copy_kernel<IdxT, MAXSEG, false, LAYER_ROWS, DEEP4, true, kWarpsPerCta>);
+  if constexpr (!LAYER_ROWS) {
+    if (e == cudaSuccess)
+      e = cudaFuncGetAttributes(
+          &a, row_copy_kernel<IdxT, MAXSEG, false, false, DEEP4, true, kWarpsPerCtaWide>);
+  }
   return e;
 }
 

@@ -89,7 +89,8 @@ def test_mla78_two_pools_full_size():
 
 
 def test_mla78_two_pools_full_size_deep_tasks():
-    # 16 CTAs per launch: the deep tasks (4 KiB, 8 chunks in flight per lane)
+    # 16 CTAs per launch: 16-warp CTAs with the deep tasks (4 KiB, 8 chunks in
+    # flight per lane)
     _run_full_size(W.mla78_dsa(), max_ctas=16)
 
 

@@ -240,9 +240,10 @@ CASES = [
 
 @pytest.mark.parametrize("case", CASES, ids=[f"R{c[2]*c[3]*c[4]}_P{c[5]}_n{c[8]}" for c in CASES])
 @pytest.mark.parametrize("where", ["device", "host"])
-@pytest.mark.parametrize("ctas", [0, 16])
+@pytest.mark.parametrize("ctas", [0, 16, 32])
 def test_ragged_backup_and_load(case, where, ctas):
-    """ctas 16: launches of 16 CTAs, which take the deep tasks (about 4 KiB each)."""
+    """ctas 16: launches of 16 CTAs of 16 warps each, with the deep tasks (about 4 KiB
+    each); ctas 32: 8-warp CTAs with the deep tasks."""
     L, T, hn, hd, ds, P, slots, pages, n, frag = case
     s = G.shape(L=L, T=T, head_num=hn, head_dim=hd, dtype_size=ds, P=P, slots=slots, pages=pages)
     pool = G.make_pool(s, seed=n)
