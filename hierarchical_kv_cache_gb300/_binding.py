@@ -27,7 +27,7 @@ HICACHE_INDEX_HOST, HICACHE_INDEX_DEVICE = 0, 1
 HICACHE_LAYOUT_PAGE_FIRST_DIRECT, HICACHE_LAYOUT_PAGE_FIRST = 0, 1
 HICACHE_OP_BACKUP, HICACHE_OP_LOAD = 0, 1
 # copy-CTA budgets below which AUTO may take the staged path (include/hicache.h)
-HICACHE_AUTO_STAGED_BELOW_CTAS_BACKUP, HICACHE_AUTO_STAGED_BELOW_CTAS_LOAD = 24, 24
+HICACHE_AUTO_STAGED_BELOW_CTAS_BACKUP, HICACHE_AUTO_STAGED_BELOW_CTAS_LOAD = 5, 5
 HICACHE_DEVERR_RANGE, HICACHE_DEVERR_PAGE_ALIGN, HICACHE_DEVERR_TIMEOUT = 1, 2, 4
 
 

@@ -591,11 +591,12 @@ hicache_path choose_path(const std::vector<PoolInfo>& pools, const hicache_opts&
   // Measured on GB300 (NVLink-C2C host link): with the SMs to itself the
   // zero-copy kernel reaches the copy-engine bandwidth and was at least as
   // fast as the staged path at every point of the row size / page size /
-  // length sweep.  Its bandwidth grows with its CTAs, though, until about 38
-  // fill the link, while the staged path needs SMs only for short gather and
-  // scatter kernels.  So when the caller caps the copy's CTAs to keep the SMs
-  // for compute, below the crossover the staged path is faster, where it may
-  // run and its DMAs are large.
+  // length sweep.  Its bandwidth grows with its CTAs, though, until about 16
+  // (of 16 warps) fill the link, while the staged path needs SMs only for
+  // short gather and scatter kernels.  So when the caller caps the copy's
+  // CTAs to keep the SMs for compute, below the crossover (5 CTAs beside a
+  // bf16 GEMM loop) the staged path is faster, where it may run and its DMAs
+  // are large.
   const int32_t below = dir == kDevToPaged ? HICACHE_AUTO_STAGED_BELOW_CTAS_BACKUP
                                            : HICACHE_AUTO_STAGED_BELOW_CTAS_LOAD;
   if (o.max_ctas <= 0 || o.max_ctas >= below) return HICACHE_PATH_ZERO_COPY;

@@ -150,12 +150,15 @@ typedef struct hicache_opts {
                               per SM for a backup, one per two SMs for a load); else caps the
                               CTAs of each copy kernel, so that compute running at the same
                               time keeps the other SMs.  Copies of up to 76 CTAs against the
-                              host pool take deep tasks (twice the bytes in flight per warp).
-                              Measured on GB300 beside a bf16 GEMM loop: 32 CTAs moved 169-200
-                              GB/s and cost the GEMM 8-20 % of its throughput, against 21-34 %
-                              with one CTA per SM.  A backup and a load-back running at the
-                              same time moved the most together with 76 on both calls (298-317
-                              GB/s, against about 245 with the defaults).  Below
+                              host pool take deep tasks (twice the bytes in flight per warp),
+                              and a cap of 16 or fewer runs 512-thread CTAs (twice the warps).
+                              Measured on GB300 beside a bf16 GEMM loop: 8 CTAs moved 123-158
+                              GB/s, 16 CTAs 178-200, and cost the GEMM 5-19 % of its
+                              throughput, against 20-32 % with one CTA per SM (backups between
+                              about 18 and 26 CTAs move less than at 16 or 32).  A backup and
+                              a load-back running at the same time moved the most together
+                              with 76 on both calls (298-317 GB/s, against about 245 with the
+                              defaults).  Below
                               HICACHE_AUTO_STAGED_BELOW_CTAS_* the AUTO path may switch to the
                               staged path (see hicache_auto_path). */
   int32_t reserved;        /* must be 0 */
@@ -305,8 +308,8 @@ hicache_status hicache_backup_all_layers_static_staging(const hicache_pool* pool
 
 /* Copy-CTA budgets (opts->max_ctas) below which HICACHE_PATH_AUTO takes the
  * staged path when it may (see hicache_auto_path), per direction. */
-#define HICACHE_AUTO_STAGED_BELOW_CTAS_BACKUP 24
-#define HICACHE_AUTO_STAGED_BELOW_CTAS_LOAD 24
+#define HICACHE_AUTO_STAGED_BELOW_CTAS_BACKUP 5
+#define HICACHE_AUTO_STAGED_BELOW_CTAS_LOAD 5
 
 /*
  * The path a call with opts->path == HICACHE_PATH_AUTO takes (host only; no
@@ -317,10 +320,11 @@ hicache_status hicache_backup_all_layers_static_staging(const hicache_pool* pool
  *            layer_end - layer_begin for a burst); ignored for a backup.
  *   Index arrays are read only when opts->index_location is HICACHE_INDEX_HOST
  *   (then they must be host memory); n pairs of index_bits bits.
- * The rule, from measurements on GB300 (zero-copy bandwidth grows with its
- * CTAs until about 38 of them fill the host link; the staged path moves its
- * bytes with the copy engine and needs SMs only for short gather and scatter
- * kernels):
+ * The rule, from measurements on GB300 beside a bf16 GEMM loop (zero-copy
+ * bandwidth grows with its CTAs until about 16 of them fill the host link;
+ * the staged path moves its bytes with the copy engine and needs SMs only for
+ * short gather and scatter kernels, which pays off under a cap of 4 CTAs or
+ * fewer):
  *   the staged path when all of these hold, else zero-copy:
  *   - opts->max_ctas is set (the caller keeps the other SMs for compute) and
  *     below HICACHE_AUTO_STAGED_BELOW_CTAS_BACKUP / _LOAD;

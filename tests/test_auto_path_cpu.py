@@ -42,7 +42,7 @@ def whole_pages(k, P=64, first_dev=0, first_host=0):
     return d, h
 
 
-def opts(max_ctas=16, staging_bytes=256 * MiB, location=hk.HICACHE_INDEX_HOST, path=0):
+def opts(max_ctas=4, staging_bytes=256 * MiB, location=hk.HICACHE_INDEX_HOST, path=0):
     o = B.c_opts(path=path, index_location=location, max_ctas=max_ctas, reserved=0)
     if staging_bytes:
         o.staging[0] = FAKE + 0x40000000
@@ -139,7 +139,7 @@ def test_explicit_paths_are_returned_as_given():
     d, h = whole_pages(8)
     p = [llama_pool()]
     assert auto(p, d, h, opts(max_ctas=0, path=ST), BACKUP) == ST
-    assert auto(p, d, h, opts(max_ctas=8, path=ZC), BACKUP) == ZC
+    assert auto(p, d, h, opts(max_ctas=2, path=ZC), BACKUP) == ZC
 
 
 def test_rejects_bad_arguments():
@@ -178,7 +178,7 @@ def test_binding_takes_numpy_host_arrays():
                    num_layers=32, head_num=8, head_dim=128, dtype_size=2, page_size=64,
                    device_slots=65536, host_pages=1024)
     staging = [_Numel(FAKE + 0x40000000), _Numel(FAKE + 0x80000000)]
-    o = hk.Opts(max_ctas=16, staging=staging)
+    o = hk.Opts(max_ctas=4, staging=staging)
     assert hk.hicache_auto_path(pool, d, h, op=BACKUP, opts=o) == ST
     assert hk.hicache_auto_path(pool, d, h, op=LOAD, layers=1, opts=o) == ZC
     assert hk.hicache_auto_path(pool, d, h, op=BACKUP) == ZC
