@@ -36,10 +36,11 @@ constexpr int kDeepMaxCtas = 76;
 // warps of deep tasks per CTA instead of 8, so that the few SMs such a cap
 // allows keep twice the bytes in flight.  Measured on GB300 beside a bf16 GEMM
 // loop, 8 CTAs: a 78-layer backup 158 against 77 GB/s, its burst 139 against
-// 69, the GEMM as fast or faster meanwhile; 16 CTAs: 178 against 157 and 196
-// against 142, the GEMM 2-5 % slower meanwhile over a shorter transfer.  Up
-// to 128 registers a thread fit 512 threads; the layer-row instances need
-// more and keep 8 warps.
+// 69, the GEMM within 1.3 % or faster meanwhile; 16 CTAs: 178 against 157 and
+// 196 against 142, the GEMM 2-5 % slower meanwhile over a shorter transfer.
+// From 20 CTAs up 16 warps cost the GEMM more per byte moved than 8.  Up to
+// 128 registers a thread fit 512 threads; the layer-row instances need more
+// and keep 8 warps.
 constexpr int kWarpsPerCtaWide = 16;
 constexpr int kWideMaxCtas = 16;
 constexpr int kMaxSegSmall = 8;     // per-layer launches: pools x tensors
