@@ -90,11 +90,11 @@ def parse_args():
                     help="measure both paths beside a bf16 GEMM loop that occupies the SMs "
                          "(the regime the staged path is for) instead")
     ap.add_argument("--contention-reps", type=int, default=3)
-    ap.add_argument("--contention-staged-ctas", default="0,38",
+    ap.add_argument("--contention-staged-ctas", default="0,4,8,16",
                     help="copy CTA caps of the staged path under --contention")
     ap.add_argument("--contention-alone-only", action="store_true",
                     help="time the transfers alone only (no GEMM loop beside them)")
-    ap.add_argument("--contention-ctas", default="16,38,76,152,304",
+    ap.add_argument("--contention-ctas", default="4,8,16,24,76,152",
                     help="copy CTA caps to measure under contention (0 = library default)")
     return ap.parse_args()
 
